@@ -1,0 +1,167 @@
+"""Seeded synthetic inputs for block-sparse attention workloads.
+
+This module only draws random numbers and lays out workload descriptions
+(shapes, segment ids, ALiBi slopes).  It holds none of the attention
+arithmetic: both the CUDA path and the CPU oracle consume what it produces,
+so the two always see bit-identical inputs.
+
+Workloads (all tensors are ``[B, H, T, D]`` contiguous, ``D`` innermost):
+
+* ``grouped_fp32``   -- grouped variate attention, fp32, B=1 H=4 D=128,
+  8 groups x 17 variates = 136 tokens, segment id = token // 17
+  (TiRex2 PR "perf: expose FlexAttention loader override", sections
+  "Performance characterization" and "Variate-attention layer": one target
+  plus 16 covariates per window, embedding 512 over four heads).
+* ``grouped_bf16``   -- the same group structure at scale, bf16,
+  4096 groups x 17 = 69632 tokens.
+* ``document_bf16``  -- document packing, bf16, B=4 H=16 D=64 T=8192,
+  document lengths uniform in [256, 2048], the last one truncated
+  (FlexAttention Guide, "Production Engineering", item 1).
+* ``causal_softcap_bf16`` -- causal + tanh soft-cap C=50, bf16, B=8 H=16
+  D=128 T=4096, inputs scaled by 2 so that the cap is active (FlexAttention
+  Guide, "The Problem" soft-capping formula and the implementation script).
+* ``window_alibi_gqa_bf16`` -- causal sliding window 1024 + ALiBi, GQA
+  32 query / 8 KV heads, D=128, T=32768.
+
+Reading of the ALiBi slopes: the slopes form the geometric sequence
+``2^(-8 (h+1) / H)`` over 0-based query heads ``h`` (Press et al., as cited
+by the FlexAttention Guide); a literal 0-based ``2^(-8h/H)`` would give
+head 0 the slope 1 and no head the slope ``2^-8``.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import numpy as np
+
+BLOCK = 128
+
+
+def standard_normal(seed: int, shape, scale: float = 1.0) -> np.ndarray:
+    """fp32 N(0, scale^2) samples from numpy's PCG64 stream for ``seed``."""
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal(size=int(np.prod(shape)), dtype=np.float32)
+    if scale != 1.0:
+        x *= np.float32(scale)
+    return x.reshape(shape)
+
+
+def round_to_bf16(x: np.ndarray) -> np.ndarray:
+    """Round fp32 values to the nearest bf16 value (ties to even), kept in fp32.
+
+    The result is exactly representable in bf16, so converting it to a bf16
+    tensor is lossless and the oracle sees the very values the GPU sees.
+    """
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    lsb = (u >> np.uint32(16)) & np.uint32(1)
+    r = (u + np.uint32(0x7FFF) + lsb) & np.uint32(0xFFFF0000)
+    return r.view(np.float32)
+
+
+def group_segments(T: int, group: int) -> np.ndarray:
+    """Segment id ``t // group`` for every token (one variate group each)."""
+    return (np.arange(T, dtype=np.int64) // group).astype(np.int32)
+
+
+def document_segments(seed: int, B: int, T: int, lo: int = 256, hi: int = 2048) -> np.ndarray:
+    """Per batch row, documents of length U{lo..hi} packed until T tokens.
+
+    Lengths are drawn from a seeded stream until they cover ``T``; the last
+    document is truncated.  Ids are 0, 1, 2, ... in packing order, so every
+    row is non-decreasing.
+    """
+    rng = np.random.default_rng(seed)
+    seg = np.empty((B, T), dtype=np.int32)
+    for b in range(B):
+        pos, doc = 0, 0
+        while pos < T:
+            n = int(rng.integers(lo, hi + 1))
+            seg[b, pos:min(T, pos + n)] = doc
+            pos += n
+            doc += 1
+    return seg
+
+
+def alibi_slopes(H: int) -> np.ndarray:
+    """Geometric ALiBi slopes ``2^(-8 (h+1) / H)`` for query heads h = 0..H-1."""
+    h = np.arange(H, dtype=np.float64)
+    return np.exp2(-8.0 * (h + 1.0) / H).astype(np.float32)
+
+
+@dataclasses.dataclass
+class Workload:
+    """A seeded synthetic attention problem (shapes, mask and score_mod)."""
+
+    name: str
+    dtype: str                 # "bf16" or "fp32"
+    B: int
+    Hq: int
+    Hkv: int
+    T: int
+    D: int
+    mask: str                  # "full" | "causal" | "sliding_window" | "document" | "prefix_lm"
+    score: str = "none"        # "none" | "softcap" | "alibi" | "rel_bias"
+    window: int = 0
+    prefix_len: int = 0
+    softcap: float = 0.0
+    group: int = 0             # document mask from token // group
+    doc_lo: int = 256
+    doc_hi: int = 2048
+    rel_max: int = 0
+    input_scale: float = 1.0
+    seed: int = 0
+    groups: Optional[int] = None   # number of independent windows (grouped workloads)
+
+    @property
+    def kv_len(self) -> int:
+        return self.T
+
+    def segments(self) -> Optional[np.ndarray]:
+        """int32 [Bs, T] segment ids for document masks, else None."""
+        if self.mask != "document":
+            return None
+        if self.group > 0:
+            return group_segments(self.T, self.group)[None, :].copy()
+        return document_segments(self.seed + 1000, self.B, self.T, self.doc_lo, self.doc_hi)
+
+    def slopes(self) -> Optional[np.ndarray]:
+        return alibi_slopes(self.Hq) if self.score == "alibi" else None
+
+    def rel_bias(self) -> Optional[np.ndarray]:
+        """fp32 [Hq, 2R+1] relative-position bias table (seeded)."""
+        if self.score != "rel_bias":
+            return None
+        return standard_normal(self.seed + 2000, (self.Hq, 2 * self.rel_max + 1), 0.5)
+
+    def qkv(self):
+        """(q, k, v) fp32 numpy arrays; bf16 workloads are pre-rounded to bf16."""
+        q = standard_normal(self.seed * 3 + 0, (self.B, self.Hq, self.T, self.D), self.input_scale)
+        k = standard_normal(self.seed * 3 + 1, (self.B, self.Hkv, self.T, self.D), self.input_scale)
+        v = standard_normal(self.seed * 3 + 2, (self.B, self.Hkv, self.T, self.D), self.input_scale)
+        if self.dtype == "bf16":
+            q, k, v = round_to_bf16(q), round_to_bf16(k), round_to_bf16(v)
+        return q, k, v
+
+    def scaled(self, **kw) -> "Workload":
+        """A copy with some fields replaced (for downscaled parity cases)."""
+        return dataclasses.replace(self, **kw)
+
+
+WORKLOADS = {
+    "grouped_fp32": Workload(
+        name="grouped_fp32", dtype="fp32", B=1, Hq=4, Hkv=4, T=136, D=128,
+        mask="document", group=17, seed=1, groups=8),
+    "grouped_bf16": Workload(
+        name="grouped_bf16", dtype="bf16", B=1, Hq=4, Hkv=4, T=69632, D=128,
+        mask="document", group=17, seed=2, groups=4096),
+    "document_bf16": Workload(
+        name="document_bf16", dtype="bf16", B=4, Hq=16, Hkv=16, T=8192, D=64,
+        mask="document", seed=3),
+    "causal_softcap_bf16": Workload(
+        name="causal_softcap_bf16", dtype="bf16", B=8, Hq=16, Hkv=16, T=4096, D=128,
+        mask="causal", score="softcap", softcap=50.0, input_scale=2.0, seed=4),
+    "window_alibi_gqa_bf16": Workload(
+        name="window_alibi_gqa_bf16", dtype="bf16", B=1, Hq=32, Hkv=8, T=32768, D=128,
+        mask="sliding_window", window=1024, score="alibi", seed=5),
+}

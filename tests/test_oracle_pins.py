@@ -1,0 +1,302 @@
+"""Pins for the fp64 CPU oracle (no GPU).
+
+Each test fixes the oracle to something other than itself: closed forms
+derived by hand, the pages' printed facts (tests/golden/page_facts.json),
+reductions to simpler cases, an independent library computation (torch CPU
+float64) for the unmasked textbook case, and invariants.  Together they are
+chosen so that a dropped scale, a flipped sign, a wrong index direction or
+an off-by-one window edge fails at least one of them.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from block_sparse_attention_fa_gb300 import synth
+
+GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "page_facts.json")))
+
+
+def _rand(shape, seed, scale=1.0):
+    return synth.standard_normal(seed, shape, scale)
+
+
+# ---------------------------------------------------------------- closed forms
+
+def test_softcap_closed_form():
+    # D = 1, scale = 2 ln 2, q = k0 = 1: s0 = 2 ln 2; with C = 2, s0 / C = ln 2 and
+    # tanh(ln 2) = (4 - 1) / (4 + 1) = 3/5, so the capped score is 6/5.  k1 = 0 gives 0.
+    q = np.ones((1, 1, 1, 1), np.float32)
+    k = np.array([1.0, 0.0], np.float32).reshape(1, 1, 2, 1)
+    v = np.array([1.0, 0.0], np.float32).reshape(1, 1, 2, 1)
+    o, lse = oracle.fwd(q, k, v, score="softcap", softcap=2.0, scale=2.0 * math.log(2.0))
+    assert o[0, 0, 0, 0] == pytest.approx(1.0 / (1.0 + math.exp(-1.2)), abs=1e-14)
+    assert lse[0, 0, 0] == pytest.approx(math.log(math.exp(1.2) + 1.0), abs=1e-14)
+
+
+def test_softcap_limits():
+    q, k, v = (_rand((1, 2, 40, 16), s, 3.0) for s in (1, 2, 3))
+    o_none, l_none = oracle.fwd(q, k, v, mask="causal")
+    o_big, l_big = oracle.fwd(q, k, v, mask="causal", score="softcap", softcap=1e30)
+    np.testing.assert_allclose(o_big, o_none, atol=1e-12)
+    np.testing.assert_allclose(l_big, l_none, atol=1e-12)
+    # |C tanh(s / C)| < C: with every key masked but itself the lse of row 0 is the capped score
+    C = 2.0
+    _, l_cap = oracle.fwd(q, k, v, mask="causal", score="softcap", softcap=C)
+    assert np.all(np.abs(l_cap[..., 0]) <= C)
+    s00 = (q[..., 0, :].astype(np.float64) * k[..., 0, :]).sum(-1) / 4.0
+    np.testing.assert_allclose(l_cap[..., 0], C * np.tanh(s00 / C), atol=1e-12)
+
+
+def test_alibi_closed_form_and_sign():
+    # q = 0 makes every raw score 0, so the weights are exp(-slope |i - j|).  With
+    # slope = ln 2 and the causal row i = 2: 2^-2, 2^-1, 1 -> 1/7, 2/7, 4/7.
+    q = np.zeros((1, 1, 3, 1), np.float32)
+    k = np.ones((1, 1, 3, 1), np.float32)
+    v = np.array([1.0, 2.0, 4.0], np.float32).reshape(1, 1, 3, 1)
+    slopes = np.array([math.log(2.0)], np.float32)
+    o, lse = oracle.fwd(q, k, v, mask="causal", score="alibi", slopes=slopes)
+    assert o[0, 0, 2, 0] == pytest.approx((1 * 1 + 2 * 2 + 4 * 4) / 7.0, abs=1e-6)   # = 3
+    assert lse[0, 0, 2] == pytest.approx(math.log(7.0 / 4.0), abs=1e-6)
+    assert o[0, 0, 1, 0] == pytest.approx((1 * 1 + 2 * 2) / 3.0, abs=1e-6)
+    assert o[0, 0, 0, 0] == pytest.approx(1.0, abs=1e-12)
+
+
+def test_alibi_uses_query_head():
+    q = np.zeros((1, 2, 2, 1), np.float32)
+    k = np.ones((1, 1, 2, 1), np.float32)
+    v = np.array([0.0, 1.0], np.float32).reshape(1, 1, 2, 1)
+    slopes = np.array([0.0, math.log(3.0)], np.float32)
+    o, _ = oracle.fwd(q, k, v, mask="full", score="alibi", slopes=slopes)
+    assert o[0, 0, 0, 0] == pytest.approx(0.5, abs=1e-12)          # head 0: slope 0, uniform
+    assert o[0, 1, 0, 0] == pytest.approx(1.0 / 4.0, abs=1e-6)     # head 1: weights 1, 1/3
+
+
+def test_rel_bias_closed_form():
+    # table over r = i - j clamped to [-1, 1]: r = -1 -> ln 1, 0 -> ln 2, +1 -> ln 4
+    q = np.zeros((1, 1, 3, 1), np.float32)
+    k = np.ones((1, 1, 3, 1), np.float32)
+    v = np.array([1.0, 10.0, 100.0], np.float32).reshape(1, 1, 3, 1)
+    table = np.log(np.array([[1.0, 2.0, 4.0]], np.float64)).astype(np.float32)
+    o, _ = oracle.fwd(q, k, v, mask="full", score="rel_bias", rel_bias=table, rel_max=1)
+    # row 0: r = 0, -1, -2 -> clamp -1 : weights 2, 1, 1 (/4)
+    assert o[0, 0, 0, 0] == pytest.approx((2 * 1 + 1 * 10 + 1 * 100) / 4.0, rel=1e-6)
+    # row 1: r = 1, 0, -1 : weights 4, 2, 1 (/7)
+    assert o[0, 0, 1, 0] == pytest.approx((4 * 1 + 2 * 10 + 1 * 100) / 7.0, rel=1e-6)
+    # row 2: r = 2 -> clamp 1, 1, 0 : weights 4, 4, 2 (/10)
+    assert o[0, 0, 2, 0] == pytest.approx((4 * 1 + 4 * 10 + 2 * 100) / 10.0, rel=1e-6)
+
+
+def test_sliding_window_edge_is_inclusive():
+    # page code: q_idx >= kv_idx and (q_idx - kv_idx) <= W.  q = 0 -> uniform weights.
+    fact = GOLDEN["sliding_window_edge"]
+    assert fact["inclusive"] is True
+    W = 2
+    T = 8
+    q = np.zeros((1, 1, T, 1), np.float32)
+    k = np.ones((1, 1, T, 1), np.float32)
+    v = np.arange(T, dtype=np.float32).reshape(1, 1, T, 1)
+    o, lse = oracle.fwd(q, k, v, mask="sliding_window", window=W)
+    assert o[0, 0, 5, 0] == pytest.approx((3 + 4 + 5) / 3.0, abs=1e-12)
+    assert lse[0, 0, 5] == pytest.approx(math.log(3.0), abs=1e-12)
+    assert o[0, 0, 1, 0] == pytest.approx(0.5, abs=1e-12)
+
+
+def test_document_and_prefix_closed_forms():
+    T = 6
+    q = np.zeros((1, 1, T, 1), np.float32)
+    k = np.ones((1, 1, T, 1), np.float32)
+    v = np.arange(T, dtype=np.float32).reshape(1, 1, T, 1)
+    seg = np.array([0, 0, 1, 1, 1, 2], np.int32)
+    o, _ = oracle.fwd(q, k, v, mask="document", seg=seg)
+    np.testing.assert_allclose(o[0, 0, :, 0], [0.5, 0.5, 3, 3, 3, 5], atol=1e-12)
+    o, _ = oracle.fwd(q, k, v, mask="prefix_lm", prefix_len=2)
+    # row 0: {0, 1}; row 1: {0, 1}; row 2: {0, 1, 2}; row 4: {0..4}
+    np.testing.assert_allclose(o[0, 0, :, 0], [0.5, 0.5, 1.0, 1.5, 2.0, 2.5], atol=1e-12)
+
+
+def test_causal_row0_attends_to_itself():
+    q, k, v = (_rand((2, 3, 50, 32), s) for s in (4, 5, 6))
+    o, lse = oracle.fwd(q, k, v, mask="causal")
+    np.testing.assert_allclose(o[:, :, 0], v[:, :, 0], atol=0)
+    s00 = (q[:, :, 0].astype(np.float64) * k[:, :, 0]).sum(-1) / math.sqrt(32)
+    np.testing.assert_allclose(lse[:, :, 0], s00, atol=1e-12)
+
+
+# ---------------------------------------------------- the unmasked textbook case
+
+def test_unmasked_equals_library_softmax_attention():
+    torch = pytest.importorskip("torch")
+    q, k, v = (_rand((2, 3, 37, 24), s) for s in (7, 8, 9))
+    o, lse = oracle.fwd(q, k, v)
+    tq, tk, tv = (torch.from_numpy(x).double() for x in (q, k, v))
+    s = tq @ tk.transpose(-1, -2) / math.sqrt(24)
+    ref = torch.softmax(s, dim=-1) @ tv
+    np.testing.assert_allclose(o, ref.numpy(), atol=1e-12)
+    np.testing.assert_allclose(lse, torch.logsumexp(s, dim=-1).numpy(), atol=1e-12)
+
+
+def test_lse_normalises_masked_rows():
+    torch = pytest.importorskip("torch")
+    q, k, v = (_rand((1, 2, 30, 8), s) for s in (10, 11, 12))
+    _, lse = oracle.fwd(q, k, v, mask="sliding_window", window=5)
+    s = torch.from_numpy(q).double() @ torch.from_numpy(k).double().transpose(-1, -2) / math.sqrt(8)
+    i = torch.arange(30)[:, None]
+    j = torch.arange(30)[None, :]
+    s = s.masked_fill(~((i >= j) & (i - j <= 5)), float("-inf"))
+    total = torch.exp(s - torch.from_numpy(lse)[..., None]).sum(-1)
+    np.testing.assert_allclose(total.numpy(), 1.0, atol=1e-12)
+
+
+# ------------------------------------------------------------------ reductions
+
+def test_group_mask_is_independent_per_group_attention():
+    G, n = 5, 17
+    T = G * n
+    q, k, v = (_rand((1, 2, T, 16), s) for s in (13, 14, 15))
+    seg = synth.group_segments(T, n)
+    o, lse = oracle.fwd(q, k, v, mask="document", seg=seg)
+    for g in range(G):
+        sl = slice(g * n, (g + 1) * n)
+        og, lg = oracle.fwd(q[:, :, sl], k[:, :, sl], v[:, :, sl])
+        np.testing.assert_allclose(o[:, :, sl], og, atol=1e-13)
+        np.testing.assert_allclose(lse[:, :, sl], lg, atol=1e-13)
+
+
+def test_mask_reductions():
+    T = 45
+    q, k, v = (_rand((1, 2, T, 8), s) for s in (16, 17, 18))
+    causal = oracle.fwd(q, k, v, mask="causal")
+    full = oracle.fwd(q, k, v, mask="full")
+    for got, want in [
+        (oracle.fwd(q, k, v, mask="sliding_window", window=T - 1), causal),
+        (oracle.fwd(q, k, v, mask="sliding_window", window=10**6), causal),
+        (oracle.fwd(q, k, v, mask="prefix_lm", prefix_len=0), causal),
+        (oracle.fwd(q, k, v, mask="prefix_lm", prefix_len=T), full),
+        (oracle.fwd(q, k, v, mask="document", seg=np.zeros(T, np.int32)), full),
+        (oracle.fwd(q, k, v, mask="causal", score="alibi", slopes=np.zeros(2, np.float32)), causal),
+        (oracle.fwd(q, k, v, mask="causal", score="rel_bias",
+                    rel_bias=np.zeros((2, 7), np.float32), rel_max=3), causal),
+    ]:
+        np.testing.assert_array_equal(got[0], want[0])
+        np.testing.assert_array_equal(got[1], want[1])
+    # a narrower window differs from causal
+    assert not np.allclose(oracle.fwd(q, k, v, mask="sliding_window", window=3)[0], causal[0])
+
+
+def test_gqa_equals_repeated_kv():
+    q = _rand((2, 8, 33, 16), 19)
+    k, v = (_rand((2, 2, 33, 16), s) for s in (20, 21))
+    o, lse = oracle.fwd(q, k, v, mask="causal")
+    kr, vr = np.repeat(k, 4, axis=1), np.repeat(v, 4, axis=1)
+    o2, lse2 = oracle.fwd(q, kr, vr, mask="causal")
+    np.testing.assert_array_equal(o, o2)
+    np.testing.assert_array_equal(lse, lse2)
+
+
+def test_constant_v_gives_constant_output():
+    q, k = (_rand((1, 2, 40, 8), s) for s in (22, 23))
+    v = np.full((1, 2, 40, 8), 1.75, np.float32)
+    o, _ = oracle.fwd(q, k, v, mask="prefix_lm", prefix_len=7)
+    np.testing.assert_allclose(o, 1.75, atol=1e-14)
+
+
+def test_rows_subset_matches_full():
+    q, k, v = (_rand((2, 4, 20, 8), s) for s in (24, 25, 26))
+    o, lse = oracle.fwd(q, k, v, mask="causal")
+    rows = np.array([0, 5, 19, 20 * 4 + 3, 2 * 4 * 20 - 1], np.int64)
+    o2, l2 = oracle.fwd(q, k, v, mask="causal", rows=rows)
+    np.testing.assert_array_equal(o.reshape(-1, 8)[rows], o2)
+    np.testing.assert_array_equal(lse.reshape(-1)[rows], l2)
+
+
+def test_fully_masked_row_is_zero_with_minus_inf_lse():
+    # a window of -1 admits no pair at all (i >= j and i - j <= -1 is never true)
+    q, k, v = (_rand((1, 1, 4, 4), s) for s in (27, 28, 29))
+    o, lse = oracle.fwd(q, k, v, mask="sliding_window", window=-1)
+    assert np.all(o == 0.0) and np.all(np.isneginf(lse))
+    # a document row whose id appears among no keys of a shorter kv range
+    seg = np.array([0, 1, 1, 1], np.int32)
+    o, lse = oracle.fwd(q, k, v, mask="document", seg=seg)
+    assert np.isfinite(lse).all()
+
+
+# ------------------------------------------------------------ the tile scan
+
+def _dense_pred(mask, T, window=0, prefix_len=0, seg=None):
+    i = np.arange(T)[:, None]
+    j = np.arange(T)[None, :]
+    if mask == "full":
+        return np.ones((T, T), bool)
+    if mask == "causal":
+        return i >= j
+    if mask == "sliding_window":
+        return (i >= j) & (i - j <= window)
+    if mask == "prefix_lm":
+        return (j < prefix_len) | (i >= j)
+    if mask == "document":
+        return seg[:, None] == seg[None, :]
+    raise ValueError(mask)
+
+
+@pytest.mark.parametrize("mask,kw", [
+    ("full", {}), ("causal", {}), ("sliding_window", {"window": 11}),
+    ("prefix_lm", {"prefix_len": 13}), ("document", {}),
+])
+@pytest.mark.parametrize("T", [8, 37, 64, 70])
+def test_block_mask_classification_on_small_tiles(mask, kw, T):
+    block = 8
+    seg = None
+    if mask == "document":
+        seg = np.sort(np.random.default_rng(T).integers(0, 6, T)).astype(np.int32)
+        kw = {"seg": seg}
+    bm = oracle.block_mask(mask=mask, B=1, H=1, q_len=T, kv_len=T, block=block, **kw)
+    pred = _dense_pred(mask, T, **{k: v for k, v in kw.items()})
+    n = (T + block - 1) // block
+    for qb in range(n):
+        part = set(bm["kv_indices"][0, 0, qb, : bm["kv_num_blocks"][0, 0, qb]].tolist())
+        full = set(bm["full_kv_indices"][0, 0, qb, : bm["full_kv_num_blocks"][0, 0, qb]].tolist())
+        assert not part & full
+        assert np.all(bm["kv_indices"][0, 0, qb, bm["kv_num_blocks"][0, 0, qb]:] == -1)
+        assert np.all(bm["full_kv_indices"][0, 0, qb, bm["full_kv_num_blocks"][0, 0, qb]:] == -1)
+        for kb in range(n):
+            tile = pred[qb * block:(qb + 1) * block, kb * block:(kb + 1) * block]
+            complete = tile.shape == (block, block)
+            if not tile.any():
+                assert kb not in part and kb not in full
+            elif complete and tile.all():
+                assert kb in full
+            else:
+                assert kb in part
+
+
+def test_block_mask_skip_fractions_from_the_pages():
+    T = GOLDEN["causal_skip_fraction"]["T"]
+    nq = T // GOLDEN["tile_size"]["value"]
+    bm = oracle.block_mask(mask="causal", B=1, H=1, q_len=T, kv_len=T)
+    visited = int(bm["kv_num_blocks"].sum() + bm["full_kv_num_blocks"].sum())
+    assert visited == nq * (nq + 1) // 2 == 2080          # lower triangle incl. diagonal
+    assert int(bm["kv_num_blocks"].sum()) == nq           # only the diagonal is partial
+    assert abs((1 - visited / nq**2) - GOLDEN["causal_skip_fraction"]["about"]) < 0.01
+
+    W = GOLDEN["sliding_window_skip_fraction"]["W"]
+    bm = oracle.block_mask(mask="sliding_window", window=W, B=1, H=1, q_len=T, kv_len=T)
+    full = int(bm["full_kv_num_blocks"].sum())
+    part = int(bm["kv_num_blocks"].sum())
+    # q-blocks 0..7 visit qb full + 1 diagonal; later ones 7 full + 2 partial
+    assert (full, part) == (28 + 56 * 7, 8 + 56 * 2) == (420, 120)
+    assert 1 - (full + part) / nq**2 > GOLDEN["sliding_window_skip_fraction"]["more_than"]
+
+
+def test_block_mask_broadcast_and_tail():
+    # B > 1 document masks give per-batch rows; a tail tile is never full
+    seg = np.stack([np.zeros(300, np.int32), (np.arange(300) // 150).astype(np.int32)])
+    bm = oracle.block_mask(mask="document", B=2, H=3, q_len=300, kv_len=300, seg=seg)
+    assert bm["kv_num_blocks"].shape == (2, 3, 3)
+    np.testing.assert_array_equal(bm["kv_num_blocks"][0, 0], [1, 1, 3])
+    np.testing.assert_array_equal(bm["full_kv_num_blocks"][0, 0], [2, 2, 0])
+    for h in range(3):
+        np.testing.assert_array_equal(bm["kv_indices"][1, h], bm["kv_indices"][1, 0])
