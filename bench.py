@@ -1,0 +1,520 @@
+#!/usr/bin/env python
+"""Benchmark of the block-sparse attention hot path on one GB300 (or N ranks).
+
+A step is one pass of the whole hot path over one batch of the synthetic
+workload: BlockMask build (fa_block_mask_build) + fused forward (fa_fwd).
+Default workload: packed grouped attention at scale (bf16, B=1, H=4, D=128,
+4096 groups x 17 variates = 69632 tokens, block-diagonal group mask).
+
+Printed on rank 0: one JSON line with
+  value        forward TFLOP/s on visited 128x128 tiles (4 r c D per tile,
+               r x c the tile's in-range rows x columns), whole job, per step
+  windows_per_s  groups (independent windows) processed per second
+  roofline     the forward kernel against the measured HBM (memory-bound
+               shapes) or bf16 tensor peak (compute-bound shapes)
+  e2e          the same metric through the public API with pinned host
+               buffers, host<->device copies inside the timed region
+  cpu_baseline the fp64 oracle on a bounded sample, on the host cores
+  workloads    the other workloads (document, causal soft-cap, window+ALiBi
+               GQA, grouped fp32) measured the same way
+L2 is flushed (256 MiB write) between timed steps; the flush is outside the
+per-step CUDA events.  ``--impl reference`` times the oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from block_sparse_attention_fa_gb300 import synth  # noqa: E402
+
+METRIC = "fwd TFLOP/s on visited blocks & % of GB300 bf16 tensor peak; windows/s grouped"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+HEADLINE = "grouped_bf16"
+SECONDARY = ["document_bf16", "causal_softcap_bf16", "window_alibi_gqa_bf16", "grouped_fp32"]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS if k in d}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------- accounting
+
+def tile_sizes(n, T):
+    return np.minimum(128, T - 128 * np.arange(n))
+
+
+def visited_flops(w, bm_np):
+    """Sum over (b, hq) of 4 r c D over the visited tiles."""
+    nq = bm_np["kv_num_blocks"].shape[-1]
+    r = tile_sizes(nq, w.T).astype(np.float64)
+    c = tile_sizes(bm_np["kv_indices"].shape[-1], w.kv_len).astype(np.float64)
+    total = 0.0
+    Bm, Hm = bm_np["kv_num_blocks"].shape[:2]
+    for b in range(Bm):
+        for h in range(Hm):
+            for qb in range(nq):
+                n1 = bm_np["kv_num_blocks"][b, h, qb]
+                n2 = bm_np["full_kv_num_blocks"][b, h, qb]
+                idx = np.concatenate([bm_np["kv_indices"][b, h, qb, :n1], bm_np["full_kv_indices"][b, h, qb, :n2]])
+                total += r[qb] * c[idx].sum()
+    reps = (w.B // Bm) * (w.Hq // Hm)
+    return 4.0 * w.D * total * reps
+
+
+def algorithmic_bytes(w):
+    """Bytes the forward must move at least: Q, K, V read, O and lse written."""
+    el = 2 if w.dtype == "bf16" else 4
+    return (w.B * w.T * w.D * el * (2 * w.Hq + 2 * w.Hkv)) + w.B * w.Hq * w.T * 4
+
+
+# -------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        if not self.lines:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm, smax, reasons, busy = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                s, m, pw = float(parts[1]), float(parts[2]), float(parts[3])
+            except ValueError:
+                continue
+            sm.append(s)
+            smax.append(m)
+            busy.append((pw, s))
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unparsed"]}
+        # samples under load: the upper half by power draw
+        busy.sort()
+        loaded = [s for _, s in busy[len(busy) // 2:]] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- GPU timing
+
+class Runner:
+    """Holds device inputs for one workload and runs build + forward."""
+
+    def __init__(self, w, device):
+        import torch
+        from block_sparse_attention_fa_gb300 import fa
+        self.torch, self.fa, self.w, self.device = torch, fa, w, device
+        t0 = time.time()
+        q, k, v = w.qkv()
+        self.host = (q, k, v)
+        self.seg = w.segments()
+        dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+        self.dt = dt
+        self.q, self.k, self.v = (torch.from_numpy(x).to(device).to(dt) for x in (q, k, v))
+        self.seg_d = torch.from_numpy(self.seg).to(device) if self.seg is not None else None
+        self.score_kw = {"score": w.score}
+        if w.score == "softcap":
+            self.score_kw["softcap"] = w.softcap
+        elif w.score == "alibi":
+            self.score_kw["alibi_slopes"] = torch.from_numpy(w.slopes()).to(device)
+        self.out = torch.empty_like(self.q)
+        self.lse = torch.empty((w.B, w.Hq, w.T), dtype=torch.float32, device=device)
+        self.ws = fa.Workspace(device)
+        self.bm = self.build()
+        self.ws.check()
+        self.bm_np = self.bm.numpy()
+        self.flops = visited_flops(w, self.bm_np)
+        self.setup_s = time.time() - t0
+
+    def build(self, stream=None):
+        w = self.w
+        Bm = self.seg.shape[0] if self.seg is not None else 1
+        return self.fa.block_mask(w.mask, Bm, 1, w.T, w.T, window=w.window, prefix_len=w.prefix_len,
+                                  seg_ids=self.seg_d, stream=stream, workspace=self.ws)
+
+    def fwd(self, bm=None, stream=None):
+        return self.fa.fwd(self.q, self.k, self.v, bm or self.bm, out=self.out, lse=self.lse,
+                           workspace=self.ws, stream=stream, **self.score_kw)
+
+    def time_steps(self, steps, warmup, flush, fwd_only=False, bm=None):
+        """Per-step CUDA-event times (ms) of build+fwd and of the fwd kernel alone."""
+        torch = self.torch
+        stream = torch.cuda.current_stream()
+        for _ in range(warmup):
+            if not fwd_only:
+                self.build()
+            self.fwd(bm)
+        torch.cuda.synchronize()
+        self.ws.check()
+        step_ms, fwd_ms = [], []
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+                torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for i in range(steps):
+            if flush is not None:
+                flush.zero_()
+            a, b, c = evs[i]
+            a.record(stream)
+            if not fwd_only:
+                self.build()
+            b.record(stream)
+            self.fwd(bm)
+            c.record(stream)
+        torch.cuda.synchronize()
+        self.ws.check()
+        for a, b, c in evs:
+            step_ms.append(a.elapsed_time(c))
+            fwd_ms.append(b.elapsed_time(c))
+        return step_ms, fwd_ms
+
+    def e2e(self, steps, warmup):
+        """Metric through the public API with pinned host buffers: H2D of the
+        step's inputs, build + forward, D2H of O and lse, every step."""
+        torch, w = self.torch, self.w
+        hq, hk, hv = (torch.from_numpy(x).to(self.dt).pin_memory() for x in self.host)
+        hseg = torch.from_numpy(self.seg).pin_memory() if self.seg is not None else None
+        ho = torch.empty(self.q.shape, dtype=self.dt).pin_memory()
+        hl = torch.empty(self.lse.shape, dtype=torch.float32).pin_memory()
+        slopes = self.score_kw.get("alibi_slopes")
+        hsl = slopes.cpu().pin_memory() if slopes is not None else None
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv) + ((hseg,) if hseg is not None else ())
+                  + ((hsl,) if hsl is not None else ()))
+        d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+
+        def one():
+            q = hq.to(self.device, non_blocking=True)
+            k = hk.to(self.device, non_blocking=True)
+            v = hv.to(self.device, non_blocking=True)
+            seg = hseg.to(self.device, non_blocking=True) if hseg is not None else None
+            kw = dict(self.score_kw)
+            if hsl is not None:
+                kw["alibi_slopes"] = hsl.to(self.device, non_blocking=True)
+            Bm = seg.shape[0] if seg is not None else 1
+            bm = self.fa.block_mask(w.mask, Bm, 1, w.T, w.T, window=w.window, prefix_len=w.prefix_len,
+                                    seg_ids=seg, workspace=self.ws)
+            o, lse = self.fa.fwd(q, k, v, bm, workspace=self.ws, **kw)
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+
+        for _ in range(warmup):
+            one()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            one()
+        torch.cuda.synchronize()
+        sec = (time.perf_counter() - t0) / steps
+        self.ws.check()
+        return sec, h2d, d2h
+
+
+def summarize(w, r, step_ms, fwd_ms, peaks, peak_src):
+    ms = statistics.median(step_ms)
+    fms = statistics.mean(fwd_ms)
+    tflops = r.flops / (ms * 1e-3) / 1e12
+    fwd_tflops = r.flops / (fms * 1e-3) / 1e12
+    bytes_ = algorithmic_bytes(w)
+    gbs = bytes_ / (fms * 1e-3) / 1e9
+    # which roofline bounds the forward: arithmetic intensity vs ridge point
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    intensity = r.flops / bytes_
+    if w.dtype == "fp32":
+        roof = {"bound": "latency", "achieved": round(fms * 1e3, 2), "peak": None, "unit": "us",
+                "frac": None, "traffic": None}
+    elif intensity < ridge:
+        roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": None}
+    else:
+        roof = {"bound": "tensor", "achieved": round(fwd_tflops, 1), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(fwd_tflops / peaks["bf16_tflops"], 4), "traffic": None}
+    roof["peak_source"] = peak_src
+    roof["kernel"] = "fwd_bf16_kernel" if w.dtype == "bf16" else "fwd_fp32_kernel"
+    roof["kernel_ms"] = round(fms, 4)
+    roof["algorithmic_bytes"] = bytes_
+    roof["visited_flops"] = r.flops
+    out = {
+        "ms_per_step": round(ms, 4),
+        "tflops": round(tflops, 2),
+        "pct_bf16_peak": round(100 * tflops / peaks["bf16_tflops"], 2),
+        "fwd_ms": round(fms, 4),
+        "fwd_tflops": round(fwd_tflops, 2),
+        "fwd_gbs": round(gbs, 1),
+        "tokens_per_s": round(w.B * w.T / (ms * 1e-3), 1),
+        "visited_tiles": int(r.bm_np["kv_num_blocks"].sum() + r.bm_np["full_kv_num_blocks"].sum()),
+        "roofline": roof,
+    }
+    if w.groups:
+        out["windows_per_s"] = round(w.groups * w.B / (ms * 1e-3), 1)
+    return out
+
+
+# ----------------------------------------------------------- CPU (oracle) side
+
+def oracle_rate(w, seconds, threads, seed=0, max_rows=None):
+    """Rows/s of the oracle on seeded random rows of the workload, sized to
+    take about `seconds` (one calibration batch first)."""
+    import oracle
+    q, k, v = w.qkv()
+    seg = w.segments()
+    kw = {"mask": w.mask, "window": w.window, "prefix_len": w.prefix_len, "seg": seg, "score": w.score,
+          "softcap": w.softcap, "slopes": w.slopes()}
+    rng = np.random.default_rng(seed)
+    total = w.B * w.Hq * w.T
+    n0 = min(total, max(threads * 4, 64))
+    rows = rng.choice(total, size=n0, replace=False).astype(np.int64)
+    t0 = time.perf_counter()
+    oracle.fwd(q, k, v, rows=rows, threads=threads, **kw)
+    dt0 = time.perf_counter() - t0
+    n = int(min(total, max(n0, n0 * seconds / max(dt0, 1e-6))))
+    if max_rows:
+        n = min(n, max_rows)
+    rows = rng.choice(total, size=n, replace=False).astype(np.int64)
+    t0 = time.perf_counter()
+    oracle.fwd(q, k, v, rows=rows, threads=threads, **kw)
+    dt = time.perf_counter() - t0
+    return n, dt, total
+
+
+def cpu_baseline(w, flops, seconds):
+    import oracle
+    threads = oracle.default_threads()
+    n, dt, total = oracle_rate(w, seconds, threads)
+    rows_per_s = n / dt
+    value = rows_per_s * (flops / total) / 1e12
+    return {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} seeded random query rows of {total} ({w.name}), full fp64 rows, "
+                      f"{dt:.1f} s; value = rows/s x visited FLOPs per row",
+            "rows_per_s": round(rows_per_s, 2)}
+
+
+# ----------------------------------------------------------------------- main
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(args, w):
+    """The reference arm: the fp64 oracle, as it stands, on the host cores."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from block_sparse_attention_fa_gb300 import fa as _fa  # noqa: F401  (not used: CPU only)
+    threads = oracle.default_threads()
+    # visited FLOPs from the oracle's own tile scan (no GPU involved)
+    seg = w.segments()
+    bm = oracle.block_mask(mask=w.mask, B=seg.shape[0] if seg is not None else 1, H=1, q_len=w.T, kv_len=w.T,
+                           window=w.window, prefix_len=w.prefix_len, seg=seg, threads=threads)
+    flops = visited_flops(w, bm)
+    per_step = max(0.5, 120.0 / max(1, args.steps + args.warmup))
+    q, k, v = w.qkv()
+    kw = {"mask": w.mask, "window": w.window, "prefix_len": w.prefix_len, "seg": seg, "score": w.score,
+          "softcap": w.softcap, "slopes": w.slopes()}
+    total = w.B * w.Hq * w.T
+    n, dt0, _ = oracle_rate(w, min(per_step, 5.0), threads)
+    rows_per_step = max(threads, int(n * per_step / max(dt0, 1e-6)))
+    rng = np.random.default_rng(1)
+    times = []
+    for s in range(args.warmup + args.steps):
+        rows = rng.choice(total, size=min(rows_per_step, total), replace=False).astype(np.int64)
+        t0 = time.perf_counter()
+        oracle.fwd(q, k, v, rows=rows, threads=threads, **kw)
+        if s >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    sec_per_row = sum(times) / (len(times) * rows_per_step)
+    value = (flops / total) / sec_per_row / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "T": w.T,
+                                        "D": w.D, "mask": w.mask, "score": w.score, "rows_per_step": rows_per_step},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{rows_per_step} seeded random query rows per step of {total}"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    if w.groups:
+        line["windows_per_s"] = w.groups * w.B * (1.0 / (sec_per_row * total))
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=HEADLINE, choices=list(synth.WORKLOADS))
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    w = synth.WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", torch.cuda.current_device())
+    peaks, peak_src = load_peaks()
+    from block_sparse_attention_fa_gb300 import fa
+    fa.load_library()
+
+    r = Runner(w, device)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(device.index) as clk:
+        step_ms, fwd_ms = r.time_steps(args.steps, args.warmup, flush)
+    torch.cuda.synchronize()
+    if world > 1:
+        t = torch.tensor([statistics.median(step_ms)], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.barrier()
+        step_ms = [float(t.item())] * len(step_ms)
+    head = summarize(w, r, step_ms, fwd_ms, peaks, peak_src)
+
+    extra = {}
+    if rank == 0 and w.name == "grouped_bf16":
+        # the dense-masked pass over the same inputs: every tile partial
+        nq = r.bm.nq
+        dense = fa.BlockMask(1, 1, w.T, w.T, "document", 0, 0, r.seg_d, device)
+        dense.kv_num_blocks.fill_(nq)
+        dense.kv_indices.copy_(torch.arange(nq, dtype=torch.int32, device=device).expand(1, 1, nq, nq))
+        dense.full_kv_num_blocks.zero_()
+        dense.full_kv_indices.fill_(-1)
+        dsteps = max(3, args.steps // 4)
+        _, dfwd = r.time_steps(dsteps, 2, flush, fwd_only=True, bm=dense)
+        dms = statistics.mean(dfwd)
+        dflops = 4.0 * w.D * w.T * w.T * w.B * w.Hq
+        extra["dense_masked_pass"] = {"fwd_ms": round(dms, 3), "tflops": round(dflops / (dms * 1e-3) / 1e12, 1),
+                                      "windows_per_s": round(w.groups / (dms * 1e-3), 1),
+                                      "speedup_block_sparse": round(dms / head["fwd_ms"], 1)}
+
+    e2e = None
+    if not args.no_e2e:
+        sec, h2d, d2h = r.e2e(max(3, args.steps // 4), 2)
+        e2e = {"value": round(r.flops / sec / 1e12, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": round(sec * 1e3, 3)}
+        if w.groups:
+            e2e["windows_per_s"] = round(w.groups * w.B / sec, 1)
+
+    secondary = {}
+    if rank == 0 and not args.no_secondary:
+        for name in SECONDARY:
+            if name == w.name:
+                continue
+            w2 = synth.WORKLOADS[name]
+            r2 = Runner(w2, device)
+            s2, f2 = r2.time_steps(args.steps, args.warmup, flush)
+            secondary[name] = summarize(w2, r2, s2, f2, peaks, peak_src)
+            del r2
+            torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        cpu = cpu_baseline(w, r.flops, args.cpu_seconds)
+
+    if rank == 0:
+        n = world
+        line = {
+            "metric": METRIC,
+            "value": round(head["tflops"] * n, 3),
+            "unit": "TFLOP/s",
+            "n_gpus": n,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": head["ms_per_step"],
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": w.dtype,
+            "data": "synthetic (seeded N(0,1) inputs, shapes of the workload)",
+            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "T": w.T, "D": w.D,
+                       "mask": w.mask, "score": w.score, "groups": w.groups,
+                       "step": "fa_block_mask_build + fa_fwd", "l2": "flushed between steps (256 MiB write, "
+                       "outside the per-step events)", "parallelism": f"replicas x{n}"},
+            "pct_bf16_peak": head["pct_bf16_peak"],
+            "windows_per_s": head.get("windows_per_s", None) and round(head["windows_per_s"] * n, 1),
+            "tokens_per_s": round(head["tokens_per_s"] * n, 1),
+            "fwd_ms": head["fwd_ms"],
+            "fwd_tflops": head["fwd_tflops"],
+            "roofline": head["roofline"],
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "gpu_launches": 2 * args.steps,
+            "clocks": clk.summary(),
+            "peaks": {"source": peak_src, **peaks},
+            "workloads": secondary,
+            **extra,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,147 @@
+// block_mask.cu -- BlockMask builder (create_block_mask for the built-in
+// mask_mods).
+//
+// FlexAttention Guide ("FlexAttention Guide: Custom Fast Attention in
+// PyTorch 2.5"), "The Core Design Principles of FlexAttention", item 3, and
+// "Systems Mechanics", 1. 128x128 Tile Block Sparsity: every 128 x 128 tile
+// is classified as full (the mask holds on every pair), empty (on none) or
+// partial, so that the forward can skip empty tiles and evaluate the mask only
+// on partial ones.
+//
+// Each built-in predicate is an inequality on i, j or i - j (or, for document
+// masks, an equality of sorted segment ids), so a tile's class follows in O(1)
+// from its corner coordinates instead of a 16384-pair scan:
+//   causal   i >= j        : some pair  <=> r1 >= c0;  all pairs <=> r0 >= c1
+//   window   0 <= i-j <= W : i - j spans [r0 - c1, r1 - c0]; some pair <=> that
+//                            range meets [0, W]; all pairs <=> it lies inside
+//   prefix   j < P or i>=j : some pair  <=> c0 < P or r1 >= c0;
+//                            all pairs  <=> c1 < P or r0 >= c1
+//   document seg[i]==seg[j]: ids are non-decreasing, so the q rows carry the
+//                            ids [seg[r0], seg[r1]] and the kv columns
+//                            [seg[c0], seg[c1]], every id in between present;
+//                            some pair <=> the ranges overlap; all pairs <=>
+//                            all four ids are equal
+// (r0..r1, c0..c1 = the tile's in-range rows and columns).  A tile is full
+// only when it is also complete (128 x 128 pairs in range).
+//
+// One CTA per (q-block, mask head, mask batch) row of tiles; its threads take
+// consecutive kv blocks, so the index writes are ascending and coalesced.  The
+// partial and full lists are compacted with a warp ballot + block prefix sum.
+// For document masks the CTA also checks that its rows' ids are
+// non-decreasing and flags the workspace otherwise.
+#include "fa_internal.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kBuildThreads = 256;
+
+struct TileClass {
+    bool any;
+    bool all;
+};
+
+__device__ __forceinline__ TileClass classify(const MaskParams& m, const int32_t* seg_row, int r0,
+                                              int r1, int c0, int c1) {
+    switch (m.kind) {
+        case FA_MASK_CAUSAL:
+            return {r1 >= c0, r0 >= c1};
+        case FA_MASK_SLIDING_WINDOW: {
+            const long long dmin = (long long)r0 - c1, dmax = (long long)r1 - c0;
+            return {dmax >= 0 && dmin <= m.window, dmin >= 0 && dmax <= m.window};
+        }
+        case FA_MASK_PREFIX_LM:
+            return {c0 < m.prefix_len || r1 >= c0, c1 < m.prefix_len || r0 >= c1};
+        case FA_MASK_DOCUMENT: {
+            const int qlo = seg_row[r0], qhi = seg_row[r1];
+            const int klo = seg_row[c0], khi = seg_row[c1];
+            return {qlo <= khi && klo <= qhi, qlo == qhi && klo == khi && qlo == klo};
+        }
+        default:  // FA_MASK_FULL
+            return {true, true};
+    }
+}
+
+__global__ void __launch_bounds__(kBuildThreads) block_mask_kernel(const BuildParams p) {
+    const int qb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int r0 = qb * kBlock;
+    const int r1 = min(r0 + kBlock - 1, p.q_len - 1);
+    const bool doc = p.mask.kind == FA_MASK_DOCUMENT;
+    const int32_t* seg_row =
+        doc ? p.mask.seg + (size_t)(p.mask.seg_batch == 1 ? 0 : b) * p.mask.seg_len : nullptr;
+
+    // Document masks need sorted ids: each segment row is checked once, by the
+    // CTAs of head 0 (and batch 0 when the row is shared), pairs (r, r + 1).
+    if (doc && h == 0 && (p.mask.seg_batch != 1 || b == 0)) {
+        const int end = min(r0 + kBlock, p.mask.seg_len - 1);
+        bool bad = false;
+        for (int r = r0 + tid; r < end; r += kBuildThreads) bad |= seg_row[r] > seg_row[r + 1];
+        if (bad && p.ws) {
+            atomicCAS(p.ws + WS_CHECK_DETAIL, 0u, (uint32_t)b + 1u);
+            atomicOr(p.ws + WS_FLAGS, WS_FLAG_CHECK);
+        }
+    }
+
+    const size_t row = ((size_t)b * p.H + h) * p.nq + qb;
+    int32_t* part_out = p.kv_indices + row * p.nkv;
+    int32_t* full_out = p.full_kv_indices + row * p.nkv;
+    const bool q_complete = (r1 - r0) == kBlock - 1;
+
+    __shared__ int warp_part[kBuildThreads / 32];
+    __shared__ int warp_full[kBuildThreads / 32];
+    int base_part = 0, base_full = 0;
+
+    for (int kb0 = 0; kb0 < p.nkv; kb0 += kBuildThreads) {
+        const int kb = kb0 + tid;
+        bool part = false, full = false;
+        if (kb < p.nkv) {
+            const int c0 = kb * kBlock;
+            const int c1 = min(c0 + kBlock - 1, p.kv_len - 1);
+            const TileClass t = classify(p.mask, seg_row, r0, r1, c0, c1);
+            const bool complete = q_complete && (c1 - c0) == kBlock - 1;
+            full = t.any && t.all && complete;
+            part = t.any && !full;
+        }
+        const unsigned bp = __ballot_sync(0xffffffffu, part);
+        const unsigned bf = __ballot_sync(0xffffffffu, full);
+        if (lane == 0) {
+            warp_part[warp] = __popc(bp);
+            warp_full[warp] = __popc(bf);
+        }
+        __syncthreads();
+        int off_part = base_part, off_full = base_full, tot_part = 0, tot_full = 0;
+#pragma unroll
+        for (int w = 0; w < kBuildThreads / 32; ++w) {
+            if (w < warp) {
+                off_part += warp_part[w];
+                off_full += warp_full[w];
+            }
+            tot_part += warp_part[w];
+            tot_full += warp_full[w];
+        }
+        const unsigned below = (1u << lane) - 1u;
+        if (part) part_out[off_part + __popc(bp & below)] = kb;
+        if (full) full_out[off_full + __popc(bf & below)] = kb;
+        base_part += tot_part;
+        base_full += tot_full;
+        __syncthreads();
+    }
+    for (int t = base_part + tid; t < p.nkv; t += kBuildThreads) part_out[t] = -1;
+    for (int t = base_full + tid; t < p.nkv; t += kBuildThreads) full_out[t] = -1;
+    if (tid == 0) {
+        p.kv_num_blocks[row] = base_part;
+        p.full_kv_num_blocks[row] = base_full;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_block_mask_build(const BuildParams& p, cudaStream_t s) {
+    const dim3 grid(p.nq, p.H, p.B);
+    block_mask_kernel<<<grid, kBuildThreads, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace fa

@@ -1,0 +1,76 @@
+// fa_internal.h -- parameter blocks and launchers shared by the host layer
+// (fa_api.cu) and the kernels (block_mask.cu, fwd_fp32.cu, fwd_bf16.cu).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/fa.h"
+
+namespace fa {
+
+constexpr int kBlock = 128;       // BlockMask tile edge (q and kv)
+
+// The BlockMask as the kernels see it.
+struct BlockMaskView {
+    int B, H;                     // mask extents (1 = broadcast)
+    int nq, nkv;
+    const int32_t* kv_num_blocks;
+    const int32_t* kv_indices;
+    const int32_t* full_kv_num_blocks;
+    const int32_t* full_kv_indices;
+};
+
+// A built-in mask_mod as the kernels see it.
+struct MaskParams {
+    int kind;                     // fa_mask_kind
+    int window;
+    int prefix_len;
+    int seg_batch;
+    const int32_t* seg;           // [seg_batch, seg_len]
+    int seg_len;
+};
+
+struct ScoreParams {
+    int kind;                     // fa_score_kind
+    float softcap;
+    const float* slopes;
+    const float* rel_bias;
+    int rel_max;
+};
+
+struct FwdParams {
+    int B, Hq, Hkv, q_len, kv_len, D, group;
+    float scale;                  // 1/sqrt(D) unless overridden
+    BlockMaskView bm;
+    MaskParams mask;
+    ScoreParams score;
+    const void* q;
+    const void* k;
+    const void* v;
+    void* o;
+    float* lse;
+    uint32_t* ws;
+    uint64_t timeout_ns;
+    uint32_t flags;
+    uint32_t debug_flags;
+};
+
+struct BuildParams {
+    int B, H, q_len, kv_len, nq, nkv;
+    MaskParams mask;
+    int32_t* kv_num_blocks;
+    int32_t* kv_indices;
+    int32_t* full_kv_num_blocks;
+    int32_t* full_kv_indices;
+    uint32_t* ws;
+};
+
+// Launchers (return the launch's cudaError_t).
+cudaError_t launch_block_mask_build(const BuildParams& p, cudaStream_t s);
+cudaError_t launch_fwd_fp32(const FwdParams& p, cudaStream_t s);
+cudaError_t launch_fwd_bf16(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, cudaStream_t s);
+
+}  // namespace fa

@@ -1,0 +1,199 @@
+// fwd_fp32.cu -- block-sparse attention forward for fp32 inputs, in fp32 FFMA.
+//
+// Same operation as the bf16 tensor-core kernel (FlexAttention Guide, "The
+// Core Design Principles of FlexAttention", items 1-3): for each visited tile
+// of the BlockMask, S = scale * Q K^T, score_mod on every element, mask_mod
+// only on partial tiles, online softmax, O += P V; then O /= l and
+// lse = m + ln l.  TF32 tensor cores round the inputs to 10 mantissa bits,
+// which alone moves O by ~1e-3, so fp32 inputs take exact fp32 FMAs here.
+//
+// CTA: 64 query rows of one (b, h, 128-row q-block), 4 threads per row; each
+// thread owns every fourth float4 of the head dimension (conflict-free shared
+// loads).  K/V are staged through shared memory 32 rows at a time.
+#include <math_constants.h>
+
+#include "fa_internal.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kRows = 64;         // query rows per CTA
+constexpr int kTpr = 4;           // threads per row
+constexpr int kThreads32 = kRows * kTpr;
+constexpr int kChunk = 32;        // kv rows per shared-memory stage
+
+template <int D, int SCORE>
+__global__ void __launch_bounds__(kThreads32) fwd_fp32_kernel(const FwdParams p) {
+    constexpr int NV = D / 4;           // float4 per row
+    constexpr int NT = NV / kTpr;       // float4 per thread
+    __shared__ float4 ks[kChunk][NV];
+    __shared__ float4 vs[kChunk][NV];
+    __shared__ int segs[kChunk];
+
+    int idx = blockIdx.x;
+    const int half = idx & 1;
+    idx >>= 1;
+    const int qb = idx % p.bm.nq;
+    idx /= p.bm.nq;
+    const int hq = idx % p.Hq;
+    const int b = idx / p.Hq;
+    const int hk = hq / p.group;
+
+    const int tid = threadIdx.x;
+    const int rl = tid / kTpr, qd = tid % kTpr;
+    const int i = qb * kBlock + half * kRows + rl;
+    const bool row_ok = i < p.q_len;
+
+    const float4* q4 = reinterpret_cast<const float4*>(p.q);
+    const float4* k4 = reinterpret_cast<const float4*>(p.k) + ((size_t)b * p.Hkv + hk) * p.kv_len * NV;
+    const float4* v4 = reinterpret_cast<const float4*>(p.v) + ((size_t)b * p.Hkv + hk) * p.kv_len * NV;
+
+    float4 qf[NT], of[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        qf[t] = row_ok ? q4[(((size_t)b * p.Hq + hq) * p.q_len + i) * NV + qd + kTpr * t]
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+        of[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+
+    const int mb = p.bm.B == 1 ? 0 : b, mh = p.bm.H == 1 ? 0 : hq;
+    const size_t mrow = ((size_t)mb * p.bm.H + mh) * p.bm.nq + qb;
+    const int n_part = p.bm.kv_num_blocks[mrow];
+    const int n = n_part + p.bm.full_kv_num_blocks[mrow];
+    const int32_t* part_idx = p.bm.kv_indices + mrow * p.bm.nkv;
+    const int32_t* full_idx = p.bm.full_kv_indices + mrow * p.bm.nkv;
+
+    const bool doc = p.mask.kind == FA_MASK_DOCUMENT;
+    const int32_t* seg_row =
+        doc ? p.mask.seg + (size_t)(p.mask.seg_batch == 1 ? 0 : b) * p.mask.seg_len : nullptr;
+    const int my_seg = (doc && row_ok) ? seg_row[i] : 0;
+    float slope = 0.f;
+    if (SCORE == FA_SCORE_ALIBI) slope = p.score.slopes[hq];
+    const float* rb = SCORE == FA_SCORE_REL_BIAS
+                          ? p.score.rel_bias + (size_t)hq * (2 * p.score.rel_max + 1)
+                          : nullptr;
+
+    float m = -CUDART_INF_F, l = 0.f;
+
+    for (int j = 0; j < n; ++j) {
+        const bool partial = j < n_part;
+        const int kb = partial ? part_idx[j] : full_idx[j - n_part];
+        for (int sub = 0; sub < kBlock / kChunk; ++sub) {
+            const int cs = kb * kBlock + sub * kChunk;
+            if (cs >= p.kv_len) break;
+            __syncthreads();
+            for (int e = tid; e < kChunk * NV; e += kThreads32) {
+                const int rr = e / NV, cc = e % NV;
+                const bool in = cs + rr < p.kv_len;
+                ks[rr][cc] = in ? k4[(size_t)(cs + rr) * NV + cc] : make_float4(0.f, 0.f, 0.f, 0.f);
+                vs[rr][cc] = in ? v4[(size_t)(cs + rr) * NV + cc] : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            if (doc && tid < kChunk) segs[tid] = cs + tid < p.kv_len ? seg_row[cs + tid] : 0;
+            __syncthreads();
+
+            float s[kChunk];
+            float mx = -CUDART_INF_F;
+#pragma unroll
+            for (int jj = 0; jj < kChunk; ++jj) {
+                float acc = 0.f;
+#pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    const float4 kv = ks[jj][qd + kTpr * t];
+                    acc = fmaf(qf[t].x, kv.x, acc);
+                    acc = fmaf(qf[t].y, kv.y, acc);
+                    acc = fmaf(qf[t].z, kv.z, acc);
+                    acc = fmaf(qf[t].w, kv.w, acc);
+                }
+                acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+                acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+                const int col = cs + jj;
+                float x = acc * p.scale;
+                if (SCORE == FA_SCORE_SOFTCAP) {
+                    x = p.score.softcap * tanhf(x / p.score.softcap);
+                } else if (SCORE == FA_SCORE_ALIBI) {
+                    x -= slope * fabsf((float)(i - col));
+                } else if (SCORE == FA_SCORE_REL_BIAS) {
+                    const int r = min(max(i - col, -p.score.rel_max), p.score.rel_max);
+                    x += rb[r + p.score.rel_max];
+                }
+                bool keep = col < p.kv_len;
+                if (partial) {
+                    switch (p.mask.kind) {
+                        case FA_MASK_CAUSAL: keep = keep && i >= col; break;
+                        case FA_MASK_SLIDING_WINDOW:
+                            keep = keep && i >= col && i - col <= p.mask.window;
+                            break;
+                        case FA_MASK_PREFIX_LM:
+                            keep = keep && (col < p.mask.prefix_len || i >= col);
+                            break;
+                        case FA_MASK_DOCUMENT: keep = keep && segs[jj] == my_seg; break;
+                        default: break;
+                    }
+                }
+                s[jj] = keep ? x : -CUDART_INF_F;
+                mx = fmaxf(mx, s[jj]);
+            }
+            const float m_new = fmaxf(m, mx);
+            if (m_new == -CUDART_INF_F) continue;      // nothing visible yet
+            const float alpha = expf(m - m_new);       // m = -inf -> 0
+            l *= alpha;
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                of[t].x *= alpha; of[t].y *= alpha; of[t].z *= alpha; of[t].w *= alpha;
+            }
+#pragma unroll
+            for (int jj = 0; jj < kChunk; ++jj) {
+                const float pj = expf(s[jj] - m_new);
+                l += pj;
+#pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    const float4 vv = vs[jj][qd + kTpr * t];
+                    of[t].x = fmaf(pj, vv.x, of[t].x);
+                    of[t].y = fmaf(pj, vv.y, of[t].y);
+                    of[t].z = fmaf(pj, vv.z, of[t].z);
+                    of[t].w = fmaf(pj, vv.w, of[t].w);
+                }
+            }
+            m = m_new;
+        }
+    }
+
+    if (!row_ok) return;
+    const bool empty = !(l > 0.f);
+    const float inv = empty ? 0.f : 1.f / l;
+    float4* o4 = reinterpret_cast<float4*>(p.o) + (((size_t)b * p.Hq + hq) * p.q_len + i) * NV;
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+        o4[qd + kTpr * t] = make_float4(of[t].x * inv, of[t].y * inv, of[t].z * inv, of[t].w * inv);
+    if (qd == 0)
+        p.lse[((size_t)b * p.Hq + hq) * p.q_len + i] = empty ? -CUDART_INF_F : m + logf(l);
+}
+
+template <int D>
+cudaError_t launch_d(const FwdParams& p, cudaStream_t s) {
+    const long long grid = (long long)p.B * p.Hq * p.bm.nq * 2;
+    switch (p.score.kind) {
+        case FA_SCORE_SOFTCAP:
+            fwd_fp32_kernel<D, FA_SCORE_SOFTCAP><<<(unsigned)grid, kThreads32, 0, s>>>(p);
+            break;
+        case FA_SCORE_ALIBI:
+            fwd_fp32_kernel<D, FA_SCORE_ALIBI><<<(unsigned)grid, kThreads32, 0, s>>>(p);
+            break;
+        case FA_SCORE_REL_BIAS:
+            fwd_fp32_kernel<D, FA_SCORE_REL_BIAS><<<(unsigned)grid, kThreads32, 0, s>>>(p);
+            break;
+        default:
+            fwd_fp32_kernel<D, FA_SCORE_NONE><<<(unsigned)grid, kThreads32, 0, s>>>(p);
+            break;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_fp32(const FwdParams& p, cudaStream_t s) {
+    return p.D == 64 ? launch_d<64>(p, s) : launch_d<128>(p, s);
+}
+
+}  // namespace fa

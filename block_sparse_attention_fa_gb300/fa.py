@@ -1,0 +1,244 @@
+"""Thin ctypes binding over the C ABI in ``include/fa.h``.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``_lib/libfa_gb300.so``.  PyTorch supplies device memory and the
+current stream.  If the library is missing or fails to load this module
+raises; there is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libfa_gb300.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE_CHECK = range(6)
+BF16, FP32 = 0, 1
+MASK_KINDS = {"full": 0, "causal": 1, "sliding_window": 2, "document": 3, "prefix_lm": 4}
+SCORE_KINDS = {"none": 0, "softcap": 1, "alibi": 2, "rel_bias": 3}
+OUT_FP32 = 1
+DEBUG_DROP_FIRST_LOAD = 1
+BLOCK = 128
+
+SYMBOLS = ("fa_workspace_bytes", "fa_block_mask_shape", "fa_block_mask_build", "fa_fwd",
+           "fa_workspace_check", "fa_last_error", "fa_version")
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"fa status {status}: {msg}")
+        self.status = status
+
+
+class MaskDesc(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("window", ctypes.c_int32), ("prefix_len", ctypes.c_int32),
+                ("seg_batch", ctypes.c_int32), ("seg_ids", ctypes.c_void_p)]
+
+
+class BlockMaskStruct(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("H", ctypes.c_int32), ("q_len", ctypes.c_int32),
+                ("kv_len", ctypes.c_int32), ("block_q", ctypes.c_int32), ("block_kv", ctypes.c_int32),
+                ("nq", ctypes.c_int32), ("nkv", ctypes.c_int32),
+                ("kv_num_blocks", ctypes.c_void_p), ("kv_indices", ctypes.c_void_p),
+                ("full_kv_num_blocks", ctypes.c_void_p), ("full_kv_indices", ctypes.c_void_p),
+                ("mask", MaskDesc)]
+
+
+class ScoreDesc(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("softcap", ctypes.c_float), ("alibi_slopes", ctypes.c_void_p),
+                ("rel_bias", ctypes.c_void_p), ("rel_max", ctypes.c_int32)]
+
+
+class FwdArgs(ctypes.Structure):
+    _fields_ = [("dtype", ctypes.c_int32), ("B", ctypes.c_int32), ("Hq", ctypes.c_int32),
+                ("Hkv", ctypes.c_int32), ("q_len", ctypes.c_int32), ("kv_len", ctypes.c_int32),
+                ("D", ctypes.c_int32), ("scale", ctypes.c_float),
+                ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("o", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+                ("timeout_ms", ctypes.c_uint32), ("flags", ctypes.c_uint32),
+                ("debug_flags", ctypes.c_uint32)]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load the C-ABI library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library not built: {path} is missing "
+                           "(run `python -m block_sparse_attention_fa_gb300.build`)")
+    h = ctypes.CDLL(path)
+    h.fa_workspace_bytes.restype = ctypes.c_size_t
+    h.fa_workspace_bytes.argtypes = []
+    h.fa_block_mask_shape.restype = ctypes.c_int
+    h.fa_block_mask_shape.argtypes = [ctypes.c_int32] * 4 + [ctypes.POINTER(ctypes.c_int32)] * 2 + \
+        [ctypes.POINTER(ctypes.c_int64)]
+    h.fa_block_mask_build.restype = ctypes.c_int
+    h.fa_block_mask_build.argtypes = [ctypes.POINTER(BlockMaskStruct), ctypes.c_void_p, ctypes.c_void_p]
+    h.fa_fwd.restype = ctypes.c_int
+    h.fa_fwd.argtypes = [ctypes.POINTER(FwdArgs), ctypes.POINTER(BlockMaskStruct),
+                         ctypes.POINTER(ScoreDesc), ctypes.c_void_p, ctypes.c_void_p]
+    h.fa_workspace_check.restype = ctypes.c_int
+    h.fa_workspace_check.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    h.fa_last_error.restype = ctypes.c_char_p
+    h.fa_last_error.argtypes = []
+    h.fa_version.restype = ctypes.c_char_p
+    h.fa_version.argtypes = []
+    _lib = h
+    return h
+
+
+def _check(status: int):
+    if status != OK:
+        raise FAError(status, load_library().fa_last_error().decode())
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+class Workspace:
+    """fa_workspace_bytes() zero-filled device bytes for status flags."""
+
+    def __init__(self, device=None):
+        n = load_library().fa_workspace_bytes()
+        self.tensor = torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+    @property
+    def ptr(self):
+        return ctypes.c_void_p(self.tensor.data_ptr())
+
+    def check(self, stream=None):
+        """Synchronise and raise FAError if a kernel flagged a device-side failure."""
+        _check(load_library().fa_workspace_check(self.ptr, _stream_ptr(stream)))
+
+
+_default_ws = {}
+
+
+def default_workspace(device) -> Workspace:
+    key = torch.device(device).index if torch.device(device).index is not None else torch.cuda.current_device()
+    if key not in _default_ws:
+        _default_ws[key] = Workspace(torch.device("cuda", key))
+    return _default_ws[key]
+
+
+class BlockMask:
+    """A BlockMask over 128 x 128 tiles (device int32 arrays + the mask_mod)."""
+
+    def __init__(self, B, H, q_len, kv_len, mask, window, prefix_len, seg_ids, device):
+        lib = load_library()
+        nq, nkv, ne = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int64()
+        _check(lib.fa_block_mask_shape(B, H, q_len, kv_len, ctypes.byref(nq), ctypes.byref(nkv), ctypes.byref(ne)))
+        self.B, self.H, self.q_len, self.kv_len = B, H, q_len, kv_len
+        self.nq, self.nkv = nq.value, nkv.value
+        self.mask, self.window, self.prefix_len = mask, window, prefix_len
+        self.seg_ids = seg_ids
+        self.kv_num_blocks = torch.empty((B, H, self.nq), dtype=torch.int32, device=device)
+        self.kv_indices = torch.empty((B, H, self.nq, self.nkv), dtype=torch.int32, device=device)
+        self.full_kv_num_blocks = torch.empty((B, H, self.nq), dtype=torch.int32, device=device)
+        self.full_kv_indices = torch.empty((B, H, self.nq, self.nkv), dtype=torch.int32, device=device)
+        s = BlockMaskStruct()
+        s.B, s.H, s.q_len, s.kv_len = B, H, q_len, kv_len
+        s.block_q = s.block_kv = BLOCK
+        s.nq, s.nkv = self.nq, self.nkv
+        s.kv_num_blocks = self.kv_num_blocks.data_ptr()
+        s.kv_indices = self.kv_indices.data_ptr()
+        s.full_kv_num_blocks = self.full_kv_num_blocks.data_ptr()
+        s.full_kv_indices = self.full_kv_indices.data_ptr()
+        s.mask.kind = MASK_KINDS[mask]
+        s.mask.window = window
+        s.mask.prefix_len = prefix_len
+        if seg_ids is not None:
+            s.mask.seg_batch = seg_ids.shape[0]
+            s.mask.seg_ids = seg_ids.data_ptr()
+        self.struct = s
+
+    def visited_tiles(self) -> int:
+        return int(self.kv_num_blocks.sum().item() + self.full_kv_num_blocks.sum().item())
+
+    def numpy(self) -> dict:
+        return {k: getattr(self, k).cpu().numpy() for k in
+                ("kv_num_blocks", "kv_indices", "full_kv_num_blocks", "full_kv_indices")}
+
+
+def block_mask(mask: str, B: int, H: int, q_len: int, kv_len: int, *, window: int = 0, prefix_len: int = 0,
+               seg_ids: Optional[torch.Tensor] = None, device=None, stream=None,
+               workspace: Optional[Workspace] = None) -> BlockMask:
+    """Build a BlockMask (fa_block_mask_build) for a built-in mask_mod."""
+    if seg_ids is not None:
+        if seg_ids.dim() == 1:
+            seg_ids = seg_ids[None]
+        if seg_ids.dtype != torch.int32 or not seg_ids.is_cuda:
+            raise ValueError("seg_ids must be a CUDA int32 tensor")
+        seg_ids = seg_ids.contiguous()
+        device = seg_ids.device
+    device = torch.device(device or "cuda")
+    bm = BlockMask(B, H, q_len, kv_len, mask, window, prefix_len, seg_ids, device)
+    ws = workspace or default_workspace(device)
+    _check(load_library().fa_block_mask_build(ctypes.byref(bm.struct), ws.ptr, _stream_ptr(stream)))
+    return bm
+
+
+def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, bm: BlockMask, *, score: str = "none",
+        softcap: float = 0.0, alibi_slopes: Optional[torch.Tensor] = None,
+        rel_bias: Optional[torch.Tensor] = None, rel_max: int = 0, scale: Optional[float] = None,
+        out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+        workspace: Optional[Workspace] = None, stream=None, timeout_ms: int = 0, debug_flags: int = 0,
+        out_fp32: bool = False):
+    """Block-sparse attention forward (fa_fwd); returns (o, lse).
+
+    ``out_fp32`` writes O in fp32 for bf16 inputs (FA_OUT_FP32)."""
+    if q.dtype == torch.bfloat16:
+        dt = BF16
+    elif q.dtype == torch.float32:
+        dt = FP32
+    else:
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    for t in (k, v):
+        if t.dtype != q.dtype:
+            raise ValueError("q, k and v must share a dtype")
+    for t in (q, k, v):
+        if not (t.is_cuda and t.is_contiguous() and t.dim() == 4):
+            raise ValueError("q, k, v must be contiguous CUDA tensors [B, H, T, D]")
+    B, Hq, Tq, D = q.shape
+    Hkv, Tkv = k.shape[1], k.shape[2]
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.float32 if out_fp32 else q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq, Tq), dtype=torch.float32, device=q.device)
+    a = FwdArgs()
+    a.dtype, a.B, a.Hq, a.Hkv, a.q_len, a.kv_len, a.D = dt, B, Hq, Hkv, Tq, Tkv, D
+    a.scale = 0.0 if scale is None else float(scale)
+    a.q, a.k, a.v, a.o, a.lse = q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr()
+    a.timeout_ms, a.debug_flags = timeout_ms, debug_flags
+    a.flags = OUT_FP32 if out_fp32 else 0
+    sc = ScoreDesc()
+    sc.kind = SCORE_KINDS[score]
+    sc.softcap = softcap
+    if alibi_slopes is not None:
+        sc.alibi_slopes = alibi_slopes.data_ptr()
+    if rel_bias is not None:
+        sc.rel_bias = rel_bias.data_ptr()
+        sc.rel_max = rel_max
+    ws = workspace or default_workspace(q.device)
+    _check(load_library().fa_fwd(ctypes.byref(a), ctypes.byref(bm.struct), ctypes.byref(sc), ws.ptr,
+                                 _stream_ptr(stream)))
+    return out, lse
+
+
+def version() -> str:
+    return load_library().fa_version().decode()

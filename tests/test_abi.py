@@ -1,0 +1,177 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+include/fa.h declares, the ctypes structs match the header's layout, and
+argument validation rejects bad calls before anything is launched."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def fa():
+    from block_sparse_attention_fa_gb300 import build, fa as fam
+    try:
+        build.build()
+    except RuntimeError as e:  # no CUDA toolkit on this host
+        pytest.skip(str(e))
+    fam.load_library()
+    return fam
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    assert declared_functions() == sorted([
+        "fa_block_mask_build", "fa_block_mask_shape", "fa_fwd", "fa_last_error", "fa_version",
+        "fa_workspace_bytes", "fa_workspace_check"])
+
+
+def test_library_exports_every_declared_symbol(fa):
+    lib = fa.load_library()
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(fa.SYMBOLS) == set(declared_functions())
+    out = subprocess.run(["nm", "-D", "--defined-only", fa.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (fa_\w+)", out))
+    assert set(declared_functions()) <= exported
+
+
+def test_struct_layout_matches_header(fa, tmp_path):
+    src = tmp_path / "layout.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include <stddef.h>
+#include "fa.h"
+#define F(T, m) printf(#T "." #m " %zu\n", offsetof(T, m));
+int main(void) {
+  printf("fa_mask_desc %zu\nfa_block_mask %zu\nfa_score_desc %zu\nfa_fwd_args %zu\n",
+         sizeof(fa_mask_desc), sizeof(fa_block_mask), sizeof(fa_score_desc), sizeof(fa_fwd_args));
+  F(fa_mask_desc, seg_ids) F(fa_block_mask, kv_num_blocks) F(fa_block_mask, full_kv_indices)
+  F(fa_block_mask, mask) F(fa_score_desc, alibi_slopes) F(fa_score_desc, rel_max)
+  F(fa_fwd_args, scale) F(fa_fwd_args, q) F(fa_fwd_args, lse) F(fa_fwd_args, timeout_ms)
+  F(fa_fwd_args, flags) F(fa_fwd_args, debug_flags)
+  return 0;
+}''')
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = dict(line.rsplit(" ", 1) for line in subprocess.run([str(exe)], capture_output=True,
+                                                               text=True, check=True).stdout.split("\n") if line)
+    got = {k: int(v) for k, v in got.items()}
+    assert got["fa_mask_desc"] == ctypes.sizeof(fa.MaskDesc)
+    assert got["fa_block_mask"] == ctypes.sizeof(fa.BlockMaskStruct)
+    assert got["fa_score_desc"] == ctypes.sizeof(fa.ScoreDesc)
+    assert got["fa_fwd_args"] == ctypes.sizeof(fa.FwdArgs)
+    pairs = {"fa_mask_desc": fa.MaskDesc, "fa_block_mask": fa.BlockMaskStruct,
+             "fa_score_desc": fa.ScoreDesc, "fa_fwd_args": fa.FwdArgs}
+    for key, off in got.items():
+        if "." in key:
+            t, m = key.split(".")
+            assert getattr(pairs[t], m).offset == off, key
+
+
+def test_shape_query(fa):
+    lib = fa.load_library()
+    nq, nkv, ne = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int64()
+    assert lib.fa_block_mask_shape(2, 3, 300, 129, ctypes.byref(nq), ctypes.byref(nkv), ctypes.byref(ne)) == fa.OK
+    assert (nq.value, nkv.value, ne.value) == (3, 2, 2 * 3 * 3 * 2)
+    assert lib.fa_block_mask_shape(0, 1, 1, 1, None, None, None) == fa.ERR_INVALID_ARG
+    assert b"extents" in lib.fa_last_error()
+    assert lib.fa_workspace_bytes() >= 16
+    assert b"sm_103a" in lib.fa_version()
+
+
+FAKE = 0x10000  # a 16-byte aligned non-NULL address; never dereferenced (validation fails first)
+
+
+def _bm(fa, **kw):
+    s = fa.BlockMaskStruct()
+    s.B, s.H, s.q_len, s.kv_len = 1, 1, 256, 256
+    s.block_q = s.block_kv = 128
+    s.nq, s.nkv = 2, 2
+    s.kv_num_blocks = s.kv_indices = s.full_kv_num_blocks = s.full_kv_indices = FAKE
+    s.mask.kind = fa.MASK_KINDS["causal"]
+    for k, v in kw.items():
+        if k.startswith("mask_"):
+            setattr(s.mask, k[5:], v)
+        else:
+            setattr(s, k, v)
+    return s
+
+
+def _args(fa, **kw):
+    a = fa.FwdArgs()
+    a.dtype, a.B, a.Hq, a.Hkv, a.q_len, a.kv_len, a.D = fa.BF16, 1, 4, 4, 256, 256, 128
+    a.q = a.k = a.v = a.o = a.lse = FAKE
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("kw,status,text", [
+    ({"block_q": 64}, "ERR_UNSUPPORTED", b"128"),
+    ({"nq": 3}, "ERR_INVALID_ARG", b"nq"),
+    ({"kv_indices": None}, "ERR_INVALID_ARG", b"non-NULL"),
+    ({"mask_kind": 9}, "ERR_INVALID_ARG", b"mask kind"),
+    ({"mask_kind": 2, "mask_window": -1}, "ERR_INVALID_ARG", b"window"),
+    ({"mask_kind": 4, "mask_prefix_len": -5}, "ERR_INVALID_ARG", b"prefix"),
+    ({"mask_kind": 3}, "ERR_INVALID_ARG", b"seg_ids"),
+    ({"mask_kind": 3, "mask_seg_ids": FAKE, "mask_seg_batch": 2}, "ERR_INVALID_ARG", b"seg_batch"),
+    ({"mask_kind": 3, "mask_seg_ids": FAKE, "mask_seg_batch": 1, "kv_len": 200, "nkv": 2},
+     "ERR_UNSUPPORTED", b"q_len == kv_len"),
+])
+def test_block_mask_build_rejects(fa, kw, status, text):
+    lib = fa.load_library()
+    bm = _bm(fa, **kw)
+    st = lib.fa_block_mask_build(ctypes.byref(bm), ctypes.c_void_p(FAKE), None)
+    assert st == getattr(fa, status)
+    assert text in lib.fa_last_error()
+
+
+def test_block_mask_build_needs_workspace(fa):
+    lib = fa.load_library()
+    assert lib.fa_block_mask_build(ctypes.byref(_bm(fa)), None, None) == fa.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw,bmkw,score,status,text", [
+    ({"D": 96}, {}, None, "ERR_UNSUPPORTED", b"head dim"),
+    ({"Hkv": 3}, {}, None, "ERR_INVALID_ARG", b"multiple"),
+    ({"dtype": 7}, {}, None, "ERR_INVALID_ARG", b"dtype"),
+    ({"q": FAKE + 8}, {}, None, "ERR_INVALID_ARG", b"aligned"),
+    ({"o": None}, {}, None, "ERR_INVALID_ARG", b"non-NULL"),
+    ({"q_len": 300}, {}, None, "ERR_INVALID_ARG", b"built for"),
+    ({"B": 2}, {"B": 3}, None, "ERR_INVALID_ARG", b"block mask B"),
+    ({}, {"H": 2}, None, "ERR_INVALID_ARG", b"block mask H"),
+    ({"flags": 4}, {}, None, "ERR_INVALID_ARG", b"flags"),
+    ({"dtype": 1, "flags": 1}, {}, None, "ERR_INVALID_ARG", b"bf16 inputs only"),
+    ({}, {}, {"kind": 1, "softcap": 0.0}, "ERR_INVALID_ARG", b"softcap"),
+    ({}, {}, {"kind": 2}, "ERR_INVALID_ARG", b"alibi"),
+    ({}, {}, {"kind": 3, "rel_max": 2}, "ERR_INVALID_ARG", b"relative bias"),
+    ({}, {}, {"kind": 8}, "ERR_INVALID_ARG", b"score kind"),
+])
+def test_fwd_rejects(fa, kw, bmkw, score, status, text):
+    lib = fa.load_library()
+    a = _args(fa, **kw)
+    bm = _bm(fa, **bmkw)
+    sc = fa.ScoreDesc()
+    for k, v in (score or {}).items():
+        setattr(sc, k, v)
+    st = lib.fa_fwd(ctypes.byref(a), ctypes.byref(bm), ctypes.byref(sc), ctypes.c_void_p(FAKE), None)
+    assert st == getattr(fa, status), lib.fa_last_error()
+    assert text in lib.fa_last_error()
+
+
+def test_fwd_rejects_null_args(fa):
+    lib = fa.load_library()
+    assert lib.fa_fwd(None, None, None, None, None) == fa.ERR_INVALID_ARG
+    a = _args(fa)
+    assert lib.fa_fwd(ctypes.byref(a), ctypes.byref(_bm(fa)), None, None, None) == fa.ERR_INVALID_ARG
+    assert b"workspace" in lib.fa_last_error()

@@ -1,0 +1,87 @@
+"""GPU BlockMask builder vs the oracle's brute-force tile scan: bit-exact on
+every array (counts, ascending indices, -1 padding), through the C ABI."""
+import numpy as np
+import pytest
+
+import oracle
+from block_sparse_attention_fa_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fa():
+    import torch
+    from block_sparse_attention_fa_gb300 import fa as fam
+    assert torch.cuda.is_available()
+    fam.load_library()
+    return fam
+
+
+def _build_both(fa, mask, B, H, q_len, kv_len, window=0, prefix_len=0, seg=None):
+    import torch
+    seg_t = torch.from_numpy(seg).cuda() if seg is not None else None
+    bm = fa.block_mask(mask, B, H, q_len, kv_len, window=window, prefix_len=prefix_len, seg_ids=seg_t)
+    fa.default_workspace(torch.device("cuda")).check()
+    got = bm.numpy()
+    want = oracle.block_mask(mask=mask, B=B, H=H, q_len=q_len, kv_len=kv_len, window=window,
+                             prefix_len=prefix_len, seg=seg)
+    for key in want:
+        np.testing.assert_array_equal(got[key], want[key], err_msg=f"{mask} {key}")
+    return got
+
+
+@pytest.mark.parametrize("T", [1, 17, 127, 128, 129, 136, 300, 1000, 2049])
+@pytest.mark.parametrize("mask,kw", [
+    ("full", {}), ("causal", {}), ("sliding_window", {"window": 0}), ("sliding_window", {"window": 127}),
+    ("sliding_window", {"window": 128}), ("sliding_window", {"window": 300}),
+    ("prefix_lm", {"prefix_len": 0}), ("prefix_lm", {"prefix_len": 200}), ("prefix_lm", {"prefix_len": 5000}),
+])
+def test_builder_matches_bruteforce(fa, T, mask, kw):
+    _build_both(fa, mask, 1, 1, T, T, **kw)
+
+
+@pytest.mark.parametrize("q_len,kv_len", [(200, 333), (333, 200), (64, 1000), (1000, 64)])
+@pytest.mark.parametrize("mask,kw", [("full", {}), ("causal", {}), ("sliding_window", {"window": 100}),
+                                     ("prefix_lm", {"prefix_len": 150})])
+def test_builder_rectangular(fa, q_len, kv_len, mask, kw):
+    _build_both(fa, mask, 1, 1, q_len, kv_len, **kw)
+
+
+@pytest.mark.parametrize("T,lo,hi,B,H", [(136, 17, 17, 1, 4), (1000, 1, 40, 2, 1), (3000, 100, 700, 3, 2),
+                                         (2048, 128, 128, 1, 1), (5000, 1, 5000, 2, 3)])
+def test_builder_documents(fa, T, lo, hi, B, H):
+    seg = synth.document_segments(T + lo + hi, B, T, lo, hi)
+    _build_both(fa, "document", B, H, T, T, seg=seg)
+
+
+def test_builder_shared_segments_broadcast(fa):
+    seg = synth.group_segments(700, 17)[None, :].copy()
+    _build_both(fa, "document", 3, 2, 700, 700, seg=seg)
+
+
+def test_builder_rejects_unsorted_segments(fa):
+    import torch
+    seg = np.zeros((2, 500), np.int32)
+    seg[1, 300:] = 1
+    seg[1, 400] = 0                       # not non-decreasing in batch row 1
+    bm = fa.block_mask("document", 2, 1, 500, 500, seg_ids=torch.from_numpy(seg).cuda())
+    with pytest.raises(fa.FAError) as ei:
+        fa.default_workspace(torch.device("cuda")).check()
+    assert ei.value.status == fa.ERR_DEVICE_CHECK
+    assert "row 1" in str(ei.value)
+    fa.default_workspace(torch.device("cuda")).check()      # cleared
+
+
+@pytest.mark.parametrize("name", list(synth.WORKLOADS))
+def test_builder_full_size_workloads(fa, name):
+    w = synth.WORKLOADS[name]
+    seg = w.segments()
+    got = _build_both(fa, w.mask, seg.shape[0] if seg is not None else 1, 1, w.T, w.T,
+                      window=w.window, prefix_len=w.prefix_len, seg=seg)
+    if name == "causal_softcap_bf16":
+        assert got["full_kv_num_blocks"].sum() == 496 and got["kv_num_blocks"].sum() == 32
+    if name == "window_alibi_gqa_bf16":
+        assert got["full_kv_num_blocks"].sum() == 1764 and got["kv_num_blocks"].sum() == 504
+    if name == "grouped_bf16":
+        assert got["full_kv_num_blocks"].sum() == 0 and got["kv_num_blocks"].sum() == 1568
