@@ -340,6 +340,19 @@ def cpu_baseline(w, flops, seconds):
 
 # ----------------------------------------------------------------------- main
 
+def max_over_ranks(x: float) -> float:
+    """Max of a per-rank scalar over all ranks (identity on one rank).  The
+    only cross-rank traffic of the benchmark: the data path has none."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -366,7 +379,7 @@ def run_reference(args, w):
           "softcap": w.softcap, "slopes": w.slopes()}
     total = w.B * w.Hq * w.T
     n, dt0, _ = oracle_rate(w, min(per_step, 5.0), threads)
-    rows_per_step = max(threads, int(n * per_step / max(dt0, 1e-6)))
+    rows_per_step = min(total, max(threads, int(n * per_step / max(dt0, 1e-6))))
     rng = np.random.default_rng(1)
     times = []
     for s in range(args.warmup + args.steps):
@@ -431,10 +444,9 @@ def main():
         step_ms, fwd_ms = r.time_steps(args.steps, args.warmup, flush)
     torch.cuda.synchronize()
     if world > 1:
-        t = torch.tensor([statistics.median(step_ms)], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        worst = max_over_ranks(statistics.median(step_ms))
         dist.barrier()
-        step_ms = [float(t.item())] * len(step_ms)
+        step_ms = [worst] * len(step_ms)
     head = summarize(w, r, step_ms, fwd_ms, peaks, peak_src)
 
     extra = {}

@@ -31,6 +31,7 @@
 // waited for (again with a limit), TMEM is freed and the kernel returns.
 #include <math_constants.h>
 
+#include "exp2_poly.h"
 #include "fa_internal.h"
 #include "ptx.cuh"
 
@@ -47,6 +48,40 @@ enum Bar { B_Q_FULL, B_K_FULL, B_K_EMPTY, B_V_FULL, B_V_EMPTY, B_S_FULL, B_P_FUL
            B_DRAIN, B_COUNT };
 enum Site : uint32_t { S_Q = 1, S_K_FULL, S_K_EMPTY, S_V_FULL, S_V_EMPTY, S_S_FULL, S_P_FULL,
                        S_O_FULL, S_DRAIN, S_LOAD_DRAIN };
+
+// Which columns of a full tile take their exponential on the FMA pipe (the
+// polynomial below) instead of the MUFU ex2 unit: columns with
+// (col % 16) < kPolyCols.  Balances the two pipes.
+constexpr int kPolyCols = 6;
+
+// 2^a for two values on the FMA pipe, a >= -125: a = n + f with n an integer
+// (rounded by adding 1.5 * 2^23) and f in [-1/2, 1/2]; 2^f by the cubic of
+// exp2_poly.h; n is added straight into the exponent field.
+__device__ __forceinline__ void exp2_poly2(float& p0, float& p1, float a0, float a1) {
+    constexpr float kShift = 12582912.0f;
+    float t0, t1, n0, n1, f0, f1, q0, q1;
+    fadd2(t0, t1, a0, a1, kShift, kShift);
+    fadd2(n0, n1, t0, t1, -kShift, -kShift);
+    ffma2(f0, f1, n0, n1, -1.f, -1.f, a0, a1);
+    ffma2(q0, q1, f0, f1, kExp2C3, kExp2C3, kExp2C2, kExp2C2);
+    ffma2(q0, q1, q0, q1, f0, f1, kExp2C1, kExp2C1);
+    ffma2(q0, q1, q0, q1, f0, f1, kExp2C0, kExp2C0);
+    p0 = __int_as_float(__float_as_int(q0) + (__float_as_int(t0) << 23));
+    p1 = __int_as_float(__float_as_int(q1) + (__float_as_int(t1) << 23));
+}
+
+// One pair of probabilities: p = 2^(x * sc - m), by MUFU or by polynomial.
+template <bool POLY>
+__device__ __forceinline__ void exp_pair(float& p0, float& p1, float x0, float x1, float sc, float nm) {
+    float a0, a1;
+    ffma2(a0, a1, x0, x1, sc, sc, nm, nm);
+    if (POLY) {
+        exp2_poly2(p0, p1, fmaxf(a0, -125.f), fmaxf(a1, -125.f));
+    } else {
+        p0 = ex2_approx(a0);
+        p1 = ex2_approx(a1);
+    }
+}
 
 template <int D>
 struct Layout {
@@ -219,7 +254,11 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
         if (SCORE == FA_SCORE_REL_BIAS) rb = p.score.rel_bias + (size_t)hq * (2 * p.score.rel_max + 1);
 
-        float m_use = -CUDART_INF_F, l = 0.f;
+        // l: sum of the fp32 probabilities (for lse); lb: sum of the same
+        // probabilities rounded to bf16, i.e. of exactly the weights that
+        // enter P V, so that O = sum p~ v / sum p~ is a consistent weighted
+        // mean (about 2.4x smaller worst-case error than dividing by l).
+        float m_use = -CUDART_INF_F, l = 0.f, lb = 0.f;
         bool ok = true;
         for (int j = 0; j < n; ++j) {
             const bool partial = j < n_part;
@@ -237,19 +276,24 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 for (int e = 0; e < 32; ++e) x[32 * c + e] = __uint_as_float(raw[e]);
             }
 
-            // score_mod on every visited element, in base-2 units.
-            const float di = static_cast<float>(i - c0);
+            // score_mod on every visited element.  Without a score_mod x stays
+            // the raw q.k and the scale (times log2 e) is folded into the
+            // exponent's FMA; otherwise x is the modified score in base-2 units.
+            float sc = 1.f;
+            if (SCORE == FA_SCORE_NONE) {
+                sc = sl2;
+            } else {
+                const float di = static_cast<float>(i - c0);
 #pragma unroll
-            for (int e = 0; e < 128; ++e) {
-                if (SCORE == FA_SCORE_NONE) {
-                    x[e] *= sl2;
-                } else if (SCORE == FA_SCORE_SOFTCAP) {
-                    x[e] = cap_out * tanhf(x[e] * cap_in);
-                } else if (SCORE == FA_SCORE_ALIBI) {
-                    x[e] = fmaf(-slope_l2, fabsf(di - static_cast<float>(e)), x[e] * sl2);
-                } else {
-                    const int rr = min(max(i - c0 - e, -p.score.rel_max), p.score.rel_max);
-                    x[e] = fmaf(__ldg(rb + rr + p.score.rel_max), kLog2e, x[e] * sl2);
+                for (int e = 0; e < 128; ++e) {
+                    if (SCORE == FA_SCORE_SOFTCAP) {
+                        x[e] = cap_out * tanhf(x[e] * cap_in);
+                    } else if (SCORE == FA_SCORE_ALIBI) {
+                        x[e] = fmaf(-slope_l2, fabsf(di - static_cast<float>(e)), x[e] * sl2);
+                    } else {
+                        const int rr = min(max(i - c0 - e, -p.score.rel_max), p.score.rel_max);
+                        x[e] = fmaf(__ldg(rb + rr + p.score.rel_max), kLog2e, x[e] * sl2);
+                    }
                 }
             }
 
@@ -283,9 +327,14 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 for (int e = 0; e < 128; ++e) x[e] = (e >= lo && e <= hi) ? x[e] : -CUDART_INF_F;
             }
 
-            float mx = x[0];
+            // row max: four independent chains of 3-input max
+            float m4[4] = {x[0], x[1], x[2], x[3]};
 #pragma unroll
-            for (int e = 1; e < 128; ++e) mx = fmaxf(mx, x[e]);
+            for (int e = 4; e < 128; e += 8) {
+#pragma unroll
+                for (int t = 0; t < 4; ++t) m4[t] = fmax3(m4[t], x[e + t], x[e + 4 + t]);
+            }
+            const float mx = fmax3(fmaxf(m4[0], m4[1]), m4[2], m4[3]) * sc;
             const float m_new = fmaxf(m_use, mx);
             bool need = false;
             if (j == 0) {
@@ -299,6 +348,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 const float alpha = need ? ex2_approx(m_use - m_new) : 1.f;
                 if (need) {
                     l *= alpha;
+                    lb *= alpha;
                     m_use = m_new;
                 }
 #pragma unroll 1
@@ -310,21 +360,34 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     tmem_st16(tO + lane_off + 16u * c, o);
                 }
             }
-            const float msafe = m_use == -CUDART_INF_F ? 0.f : m_use;
-            float rs = 0.f;
+            const float nm = m_use == -CUDART_INF_F ? 0.f : -m_use;
+
+            // P = 2^(x sc - m) -> bf16 pairs into TMEM over S; the row sums are
+            // kept in pairs (packed adds): rs of the fp32 values, rb of the
+            // bf16-rounded ones.  Full tiles take part of their exponentials on
+            // the FMA pipe; partial tiles (which hold -inf) all on MUFU.
+            float rs[4] = {0.f, 0.f, 0.f, 0.f}, rbs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 uint32_t pk[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    const float p0 = ex2_approx(x[64 * c + 2 * e] - msafe);
-                    const float p1 = ex2_approx(x[64 * c + 2 * e + 1] - msafe);
-                    rs += p0 + p1;
+                    const int col = 64 * c + 2 * e;
+                    float p0, p1;
+                    if (!partial && (col % 16) < kPolyCols)
+                        exp_pair<true>(p0, p1, x[col], x[col + 1], sc, nm);
+                    else
+                        exp_pair<false>(p0, p1, x[col], x[col + 1], sc, nm);
+                    const int a = (e & 1) * 2;
+                    fadd2(rs[a], rs[a + 1], rs[a], rs[a + 1], p0, p1);
                     pk[e] = pack_bf16x2(p0, p1);
+                    fadd2(rbs[a], rbs[a + 1], rbs[a], rbs[a + 1], __uint_as_float(pk[e] << 16),
+                          __uint_as_float(pk[e] & 0xffff0000u));
                 }
                 tmem_st32(tP + lane_off + 32u * c, pk);
             }
-            l += rs;
+            l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+            lb += (rbs[0] + rbs[1]) + (rbs[2] + rbs[3]);
             tc_fence_before();
             mbar_arrive(bar(B_P_FULL));
         }
@@ -333,7 +396,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         if (ok) {
             if (n > 0) tc_fence_after();
             const bool empty = !(l > 0.f);
-            const float inv = empty ? 0.f : 1.f / l;
+            const float inv = empty ? 0.f : 1.f / lb;
             const bool row_ok = i < p.q_len;
             const bool out32 = (p.flags & FA_OUT_FP32) != 0;
             const size_t row_elem = (((size_t)b * p.Hq + hq) * p.q_len + i) * D;
