@@ -17,8 +17,10 @@ Printed on rank 0: one JSON line with
   cpu_baseline the fp64 oracle on a bounded sample, on the host cores
   workloads    the other workloads (document, causal soft-cap, window+ALiBi
                GQA, grouped fp32) measured the same way
-L2 is flushed (256 MiB write) between timed steps; the flush is outside the
-per-step CUDA events.  ``--impl reference`` times the oracle instead.
+Each timed step is one replay of a CUDA graph holding the two launches, with
+CUDA events around it on the launching stream; L2 is flushed (256 MiB write)
+before every step, outside the events.  ``--impl reference`` times the oracle
+instead.
 """
 from __future__ import annotations
 
@@ -178,45 +180,57 @@ class Runner:
         self.flops = visited_flops(w, self.bm_np)
         self.setup_s = time.time() - t0
 
-    def build(self, stream=None):
+    def build(self):
         w = self.w
         Bm = self.seg.shape[0] if self.seg is not None else 1
         return self.fa.block_mask(w.mask, Bm, 1, w.T, w.T, window=w.window, prefix_len=w.prefix_len,
-                                  seg_ids=self.seg_d, stream=stream, workspace=self.ws)
+                                  seg_ids=self.seg_d, workspace=self.ws)
 
-    def fwd(self, bm=None, stream=None):
+    def fwd(self, bm=None):
         return self.fa.fwd(self.q, self.k, self.v, bm or self.bm, out=self.out, lse=self.lse,
-                           workspace=self.ws, stream=stream, **self.score_kw)
+                           workspace=self.ws, **self.score_kw)
 
-    def time_steps(self, steps, warmup, flush, fwd_only=False, bm=None):
-        """Per-step CUDA-event times (ms) of build+fwd and of the fwd kernel alone."""
+    def graph(self, fn):
+        """Capture fn (our C-ABI launches only, no allocation) in a CUDA graph,
+        so a timed step costs one graph launch of host time."""
+        torch = self.torch
+        side = torch.cuda.Stream(device=self.device)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            fn()
+            fn()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        self.ws.check()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        return g
+
+    def time_graph(self, g, steps, warmup, flush):
+        """Per-step CUDA-event times (ms) of graph replays, L2 flushed before each."""
         torch = self.torch
         stream = torch.cuda.current_stream()
         for _ in range(warmup):
-            if not fwd_only:
-                self.build()
-            self.fwd(bm)
+            g.replay()
         torch.cuda.synchronize()
-        self.ws.check()
-        step_ms, fwd_ms = [], []
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-                torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-        for i in range(steps):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for a, c in evs:
             if flush is not None:
                 flush.zero_()
-            a, b, c = evs[i]
             a.record(stream)
-            if not fwd_only:
-                self.build()
-            b.record(stream)
-            self.fwd(bm)
+            g.replay()
             c.record(stream)
         torch.cuda.synchronize()
         self.ws.check()
-        for a, b, c in evs:
-            step_ms.append(a.elapsed_time(c))
-            fwd_ms.append(b.elapsed_time(c))
-        return step_ms, fwd_ms
+        return [a.elapsed_time(c) for a, c in evs]
+
+    def time_steps(self, steps, warmup, flush):
+        """(step times, forward-kernel times) in ms: a step is BlockMask build
+        + forward; the forward is also timed alone (the dominant kernel)."""
+        step_g = self.graph(lambda: (self.bm.rebuild(workspace=self.ws), self.fwd()))
+        fwd_g = self.graph(lambda: self.fwd())
+        return self.time_graph(step_g, steps, warmup, flush), self.time_graph(fwd_g, steps, warmup, flush)
 
     def e2e(self, steps, warmup):
         """Metric through the public API with pinned host buffers: H2D of the
@@ -459,8 +473,8 @@ def main():
         dense.full_kv_num_blocks.zero_()
         dense.full_kv_indices.fill_(-1)
         dsteps = max(3, args.steps // 4)
-        _, dfwd = r.time_steps(dsteps, 2, flush, fwd_only=True, bm=dense)
-        dms = statistics.mean(dfwd)
+        dg = r.graph(lambda: r.fwd(dense))
+        dms = statistics.mean(r.time_graph(dg, dsteps, 2, flush))
         dflops = 4.0 * w.D * w.T * w.T * w.B * w.Hq
         extra["dense_masked_pass"] = {"fwd_ms": round(dms, 3), "tflops": round(dflops / (dms * 1e-3) / 1e12, 1),
                                       "windows_per_s": round(w.groups / (dms * 1e-3), 1),
@@ -507,8 +521,8 @@ def main():
             "data": "synthetic (seeded N(0,1) inputs, shapes of the workload)",
             "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "T": w.T, "D": w.D,
                        "mask": w.mask, "score": w.score, "groups": w.groups,
-                       "step": "fa_block_mask_build + fa_fwd", "l2": "flushed between steps (256 MiB write, "
-                       "outside the per-step events)", "parallelism": f"replicas x{n}"},
+                       "step": "fa_block_mask_build + fa_fwd (one CUDA graph replay)",
+                       "l2": "flushed between steps (256 MiB write, outside the per-step events)", "parallelism": f"replicas x{n}"},
             "pct_bf16_peak": head["pct_bf16_peak"],
             "windows_per_s": head.get("windows_per_s", None) and round(head["windows_per_s"] * n, 1),
             "tokens_per_s": round(head["tokens_per_s"] * n, 1),

@@ -233,6 +233,7 @@ fa_status fa_fwd(const fa_fwd_args* a, const fa_block_mask* bm, const fa_score_d
     p.kv_len = a->kv_len;
     p.D = a->D;
     p.group = a->Hq / a->Hkv;
+    p.num_units = (int)units;
     p.scale = a->scale > 0.f ? a->scale : 1.0f / std::sqrt((float)a->D);
     p.bm = {bm->B, bm->H, bm->nq, bm->nkv, bm->kv_num_blocks, bm->kv_indices, bm->full_kv_num_blocks,
             bm->full_kv_indices};

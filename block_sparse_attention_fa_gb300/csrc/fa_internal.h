@@ -42,6 +42,7 @@ struct ScoreParams {
 
 struct FwdParams {
     int B, Hq, Hkv, q_len, kv_len, D, group;
+    int num_units;                // B * Hq * nq work units
     float scale;                  // 1/sqrt(D) unless overridden
     BlockMaskView bm;
     MaskParams mask;

@@ -7,9 +7,12 @@
 // lse = m + ln l.  TF32 tensor cores round the inputs to 10 mantissa bits,
 // which alone moves O by ~1e-3, so fp32 inputs take exact fp32 FMAs here.
 //
-// CTA: 64 query rows of one (b, h, 128-row q-block), 4 threads per row; each
-// thread owns every fourth float4 of the head dimension (conflict-free shared
-// loads).  K/V are staged through shared memory 32 rows at a time.
+// CTA: 16 query rows of one (b, h, 128-row q-block), 16 threads per row; each
+// thread owns every sixteenth float4 of the head dimension (conflict-free
+// shared loads) and the 16 partial dot products meet by xor-shuffles.  Eight
+// CTAs cover a q-block, so even a 136-token problem spreads over 64 CTAs.
+// K/V are staged through shared memory 32 rows at a time, every load of a
+// stage issued before the first is used.
 #include <math_constants.h>
 
 #include "fa_internal.h"
@@ -18,8 +21,9 @@
 namespace fa {
 namespace {
 
-constexpr int kRows = 64;         // query rows per CTA
-constexpr int kTpr = 4;           // threads per row
+constexpr int kRows = 16;         // query rows per CTA
+constexpr int kTpr = 16;          // threads per row
+constexpr int kSplit = kBlock / kRows;   // CTAs per q-block
 constexpr int kThreads32 = kRows * kTpr;
 constexpr int kChunk = 32;        // kv rows per shared-memory stage
 
@@ -32,8 +36,8 @@ __global__ void __launch_bounds__(kThreads32) fwd_fp32_kernel(const FwdParams p)
     __shared__ int segs[kChunk];
 
     int idx = blockIdx.x;
-    const int half = idx & 1;
-    idx >>= 1;
+    const int part = idx % kSplit;
+    idx /= kSplit;
     const int qb = idx % p.bm.nq;
     idx /= p.bm.nq;
     const int hq = idx % p.Hq;
@@ -42,7 +46,8 @@ __global__ void __launch_bounds__(kThreads32) fwd_fp32_kernel(const FwdParams p)
 
     const int tid = threadIdx.x;
     const int rl = tid / kTpr, qd = tid % kTpr;
-    const int i = qb * kBlock + half * kRows + rl;
+    const int i = qb * kBlock + part * kRows + rl;
+    if (qb * kBlock + part * kRows >= p.q_len) return;     // the whole CTA is past the last row
     const bool row_ok = i < p.q_len;
 
     const float4* q4 = reinterpret_cast<const float4*>(p.q);
@@ -83,11 +88,22 @@ __global__ void __launch_bounds__(kThreads32) fwd_fp32_kernel(const FwdParams p)
             const int cs = kb * kBlock + sub * kChunk;
             if (cs >= p.kv_len) break;
             __syncthreads();
-            for (int e = tid; e < kChunk * NV; e += kThreads32) {
-                const int rr = e / NV, cc = e % NV;
-                const bool in = cs + rr < p.kv_len;
-                ks[rr][cc] = in ? k4[(size_t)(cs + rr) * NV + cc] : make_float4(0.f, 0.f, 0.f, 0.f);
-                vs[rr][cc] = in ? v4[(size_t)(cs + rr) * NV + cc] : make_float4(0.f, 0.f, 0.f, 0.f);
+            {
+                constexpr int kPer = kChunk * NV / kThreads32;      // float4 of K (and of V) per thread
+                float4 kr[kPer], vr[kPer];
+#pragma unroll
+                for (int t = 0; t < kPer; ++t) {
+                    const int e = tid + t * kThreads32, rr = e / NV, cc = e % NV;
+                    const bool in = cs + rr < p.kv_len;
+                    kr[t] = in ? k4[(size_t)(cs + rr) * NV + cc] : make_float4(0.f, 0.f, 0.f, 0.f);
+                    vr[t] = in ? v4[(size_t)(cs + rr) * NV + cc] : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int t = 0; t < kPer; ++t) {
+                    const int e = tid + t * kThreads32, rr = e / NV, cc = e % NV;
+                    ks[rr][cc] = kr[t];
+                    vs[rr][cc] = vr[t];
+                }
             }
             if (doc && tid < kChunk) segs[tid] = cs + tid < p.kv_len ? seg_row[cs + tid] : 0;
             __syncthreads();
@@ -105,8 +121,8 @@ __global__ void __launch_bounds__(kThreads32) fwd_fp32_kernel(const FwdParams p)
                     acc = fmaf(qf[t].z, kv.z, acc);
                     acc = fmaf(qf[t].w, kv.w, acc);
                 }
-                acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-                acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+#pragma unroll
+                for (int o = 1; o < kTpr; o <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
                 const int col = cs + jj;
                 float x = acc * p.scale;
                 if (SCORE == FA_SCORE_SOFTCAP) {
@@ -172,7 +188,7 @@ __global__ void __launch_bounds__(kThreads32) fwd_fp32_kernel(const FwdParams p)
 
 template <int D>
 cudaError_t launch_d(const FwdParams& p, cudaStream_t s) {
-    const long long grid = (long long)p.B * p.Hq * p.bm.nq * 2;
+    const long long grid = (long long)p.B * p.Hq * p.bm.nq * kSplit;
     switch (p.score.kind) {
         case FA_SCORE_SOFTCAP:
             fwd_fp32_kernel<D, FA_SCORE_SOFTCAP><<<(unsigned)grid, kThreads32, 0, s>>>(p);

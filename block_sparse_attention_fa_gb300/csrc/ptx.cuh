@@ -57,6 +57,8 @@ enum : uint32_t {
     WS_FLAGS = 0,         // bit 0: device input check failed, bit 1: wait timed out
     WS_TIMEOUT_SITE = 1,  // first wait site that ran out of time
     WS_CHECK_DETAIL = 2,  // first batch row whose segment ids are not sorted
+    WS_SCHED_NEXT = 4,    // forward: next work unit to hand out (0 between launches)
+    WS_SCHED_DONE = 5,    // forward: CTAs finished (0 between launches)
     WS_WORDS = 64
 };
 enum : uint32_t { WS_FLAG_CHECK = 1u, WS_FLAG_TIMEOUT = 2u };

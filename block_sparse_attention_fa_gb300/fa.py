@@ -129,10 +129,17 @@ class Workspace:
 _default_ws = {}
 
 
-def default_workspace(device) -> Workspace:
-    key = torch.device(device).index if torch.device(device).index is not None else torch.cuda.current_device()
+def default_workspace(device, stream=None) -> Workspace:
+    """The binding's workspace for (device, stream).  Launches that may run
+    concurrently must not share a workspace (the forward keeps its work
+    queue there), so each stream gets its own."""
+    dev = torch.device(device)
+    idx = dev.index if dev.index is not None else torch.cuda.current_device()
+    if stream is None:
+        stream = torch.cuda.current_stream(idx)
+    key = (idx, stream.cuda_stream)
     if key not in _default_ws:
-        _default_ws[key] = Workspace(torch.device("cuda", key))
+        _default_ws[key] = Workspace(torch.device("cuda", idx))
     return _default_ws[key]
 
 
@@ -167,6 +174,14 @@ class BlockMask:
             s.mask.seg_ids = seg_ids.data_ptr()
         self.struct = s
 
+    def rebuild(self, stream=None, workspace: Optional["Workspace"] = None):
+        """Run fa_block_mask_build again into this BlockMask's own buffers
+        (e.g. after the segment ids changed in place); capturable in a CUDA
+        graph since it allocates nothing."""
+        ws = workspace or default_workspace(self.kv_num_blocks.device, stream)
+        _check(load_library().fa_block_mask_build(ctypes.byref(self.struct), ws.ptr, _stream_ptr(stream)))
+        return self
+
     def visited_tiles(self) -> int:
         return int(self.kv_num_blocks.sum().item() + self.full_kv_num_blocks.sum().item())
 
@@ -188,7 +203,7 @@ def block_mask(mask: str, B: int, H: int, q_len: int, kv_len: int, *, window: in
         device = seg_ids.device
     device = torch.device(device or "cuda")
     bm = BlockMask(B, H, q_len, kv_len, mask, window, prefix_len, seg_ids, device)
-    ws = workspace or default_workspace(device)
+    ws = workspace or default_workspace(device, stream)
     _check(load_library().fa_block_mask_build(ctypes.byref(bm.struct), ws.ptr, _stream_ptr(stream)))
     return bm
 
@@ -234,7 +249,7 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, bm: BlockMask, *, sco
     if rel_bias is not None:
         sc.rel_bias = rel_bias.data_ptr()
         sc.rel_max = rel_max
-    ws = workspace or default_workspace(q.device)
+    ws = workspace or default_workspace(q.device, stream)
     _check(load_library().fa_fwd(ctypes.byref(a), ctypes.byref(bm.struct), ctypes.byref(sc), ws.ptr,
                                  _stream_ptr(stream)))
     return out, lse

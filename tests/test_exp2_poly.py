@@ -1,4 +1,4 @@
-"""The polynomial 2^x used on the FMA pipe: its header matches a fresh Remez
+"""The polynomials evaluated on the FMA pipe.  For 2^x: its header matches a fresh Remez
 derivation, and the evaluation scheme (round-to-integer by adding 1.5*2^23,
 degree-3 polynomial on [-1/2, 1/2], integer add into the exponent field),
 carried out in fp32 on the CPU, stays within 1e-4 relative error of exp2
@@ -14,7 +14,7 @@ CSRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
 
 
 def _gen():
-    spec = importlib.util.spec_from_file_location("gen_exp2_poly", os.path.join(CSRC, "gen_exp2_poly.py"))
+    spec = importlib.util.spec_from_file_location("gen_poly", os.path.join(CSRC, "gen_poly.py"))
     m = importlib.util.module_from_spec(spec)
     spec.loader.exec_module(m)
     return m
@@ -26,7 +26,7 @@ def header_coeffs():
 
 
 def test_header_matches_derivation():
-    c, maxerr, _ = _gen().remez(3)
+    c, maxerr = _gen().exp2_coeffs(3)
     np.testing.assert_allclose(header_coeffs(), np.float32(c), rtol=0, atol=1e-7)
     assert maxerr < 1e-4
 
@@ -52,3 +52,39 @@ def test_relative_error_over_the_softmax_range():
     want = np.exp2(x.astype(np.float64))
     rel = np.abs(got - want) / want
     assert rel.max() < 1e-4, rel.max()
+
+
+def tanh_header():
+    text = open(os.path.join(CSRC, "tanh_poly.h")).read()
+    c = [float(v) for v in re.findall(r"kTanhC\d = ([-0-9.e]+)f;", text)]
+    U = float(re.search(r"kTanhRange = ([-0-9.e]+)f;", text).group(1))
+    return c, U
+
+
+def test_tanh_header_matches_derivation():
+    g = _gen()
+    c, maxerr = g.tanh_coeffs()
+    hc, U = tanh_header()
+    assert U == g.TANH_RANGE
+    np.testing.assert_allclose(hc, np.float32(c), rtol=0, atol=1e-7)
+    assert maxerr < 1e-5
+
+
+def test_softcap_polynomial_as_the_kernel_folds_it():
+    """x = s * Q(s^2) with Q_k = C log2(e) a c_k a^(2k), a = scale / C: the
+    capped score in base-2 units, in fp32, within 2e-5 relative of
+    C tanh(scale s / C) log2(e) wherever |scale s / C| <= U."""
+    hc, U = tanh_header()
+    log2e = 1.4426950408889634
+    for C, scale in [(50.0, 128 ** -0.5), (5.0, 64 ** -0.5), (1.0, 1.0)]:
+        a = np.float32(scale / C)
+        Q = [np.float32(C * log2e * a * ck * float(a) ** (2 * k)) for k, ck in enumerate(hc)]
+        s = np.linspace(-U / a, U / a, 400001).astype(np.float32)
+        w = (s * s).astype(np.float32)
+        q = Q[4]
+        for k in (3, 2, 1, 0):
+            q = np.float32(np.float64(q) * np.float64(w) + np.float64(Q[k]))
+        x = (s * q).astype(np.float64)
+        want = C * np.tanh(np.float64(scale) * s / C) * log2e
+        nz = np.abs(want) > 0
+        assert np.max(np.abs(x[nz] - want[nz]) / np.abs(want[nz])) < 2e-5
