@@ -131,6 +131,11 @@ fa_status make_tmap(CUtensorMap* map, const void* base, int B, int H, int T, int
 
 }  // namespace
 
+fa_status fa::report(fa_status st, const char* msg) {
+    g_last_error = msg;
+    return st;
+}
+
 extern "C" {
 
 const char* fa_last_error(void) { return g_last_error.c_str(); }

@@ -68,6 +68,9 @@ struct BuildParams {
     uint32_t* ws;
 };
 
+// Sets this thread's fa_last_error() message and returns `st`.
+fa_status report(fa_status st, const char* msg);
+
 // Launchers (return the launch's cudaError_t).
 cudaError_t launch_block_mask_build(const BuildParams& p, cudaStream_t s);
 cudaError_t launch_fwd_fp32(const FwdParams& p, cudaStream_t s);

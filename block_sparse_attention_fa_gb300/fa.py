@@ -25,7 +25,7 @@ DEBUG_DROP_FIRST_LOAD = 1
 BLOCK = 128
 
 SYMBOLS = ("fa_workspace_bytes", "fa_block_mask_shape", "fa_block_mask_build", "fa_fwd",
-           "fa_workspace_check", "fa_last_error", "fa_version")
+           "fa_fwd_noalloc", "fa_workspace_check", "fa_last_error", "fa_version")
 
 
 class FAError(RuntimeError):
@@ -85,6 +85,9 @@ def load_library(path: str = LIB_PATH):
     h.fa_fwd.restype = ctypes.c_int
     h.fa_fwd.argtypes = [ctypes.POINTER(FwdArgs), ctypes.POINTER(BlockMaskStruct),
                          ctypes.POINTER(ScoreDesc), ctypes.c_void_p, ctypes.c_void_p]
+    h.fa_fwd_noalloc.restype = ctypes.c_int
+    h.fa_fwd_noalloc.argtypes = [ctypes.POINTER(FwdArgs), ctypes.POINTER(BlockMaskStruct),
+                                 ctypes.POINTER(ScoreDesc), ctypes.c_void_p]
     h.fa_workspace_check.restype = ctypes.c_int
     h.fa_workspace_check.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
     h.fa_last_error.restype = ctypes.c_char_p
@@ -252,6 +255,35 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, bm: BlockMask, *, sco
     ws = workspace or default_workspace(q.device, stream)
     _check(load_library().fa_fwd(ctypes.byref(a), ctypes.byref(bm.struct), ctypes.byref(sc), ws.ptr,
                                  _stream_ptr(stream)))
+    return out, lse
+
+
+def fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, bm: BlockMask, *, out: torch.Tensor,
+                lse: torch.Tensor, score: str = "none", softcap: float = 0.0,
+                alibi_slopes: Optional[torch.Tensor] = None, rel_bias: Optional[torch.Tensor] = None,
+                rel_max: int = 0, scale: Optional[float] = None, stream=None, out_fp32: bool = False):
+    """fa_fwd_noalloc: the forward for callers that cannot allocate device
+    memory.  The caller passes preallocated `out` and `lse`; no workspace is
+    taken (the library's scratch is a static device array)."""
+    dt = {torch.bfloat16: BF16, torch.float32: FP32}.get(q.dtype)
+    if dt is None:
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    B, Hq, Tq, D = q.shape
+    a = FwdArgs()
+    a.dtype, a.B, a.Hq, a.Hkv, a.q_len, a.kv_len, a.D = dt, B, Hq, k.shape[1], Tq, k.shape[2], D
+    a.scale = 0.0 if scale is None else float(scale)
+    a.q, a.k, a.v, a.o, a.lse = q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr()
+    a.flags = OUT_FP32 if out_fp32 else 0
+    sc = ScoreDesc()
+    sc.kind = SCORE_KINDS[score]
+    sc.softcap = softcap
+    if alibi_slopes is not None:
+        sc.alibi_slopes = alibi_slopes.data_ptr()
+    if rel_bias is not None:
+        sc.rel_bias = rel_bias.data_ptr()
+        sc.rel_max = rel_max
+    _check(load_library().fa_fwd_noalloc(ctypes.byref(a), ctypes.byref(bm.struct), ctypes.byref(sc),
+                                         _stream_ptr(stream)))
     return out, lse
 
 

@@ -183,6 +183,28 @@ fa_status fa_block_mask_build(const fa_block_mask *bm, void *workspace, void *st
 fa_status fa_fwd(const fa_fwd_args *a, const fa_block_mask *bm, const fa_score_desc *sc,
                  void *workspace, void *stream);
 
+/* fa_fwd for callers that cannot allocate device memory: code that runs
+ * inside a device-memory allocator's own hooks, processes whose device memory
+ * a framework hands out in full and forbids side allocations from, and paths
+ * that must not call cudaMalloc because it can synchronise the device.  The
+ * source pages have no counterpart to this entry point; it is this library's
+ * own.  The caller passes inputs and outputs as for fa_fwd, but no workspace:
+ * the status words live in a static, 256-byte aligned __device__ array of
+ * 4 KiB that every GPU loading the library holds until the process exits.
+ *   - The first call on a device looks up that array's device address
+ *     (cudaGetSymbolAddress, with the device current); make that first call
+ *     before any stream capture.
+ *   - Every call clears the status words on `stream` before its launch.  All
+ *     calls share the array, so calls whose work can overlap on the GPU
+ *     (unordered streams) race on it.
+ *   - A device-side wait that runs out of time still ends the kernel cleanly,
+ *     but is not reported here; use fa_fwd with a workspace where that matters.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ * Returns what fa_fwd returns for the same arguments, or FA_ERR_UNSUPPORTED
+ * if the forward needs more scratch than the static maximum.               */
+fa_status fa_fwd_noalloc(const fa_fwd_args *a, const fa_block_mask *bm, const fa_score_desc *sc,
+                         void *stream);
+
 /* Synchronise `stream`, then report and clear the device-side flags in
  * `workspace`: FA_OK, FA_ERR_TIMEOUT or FA_ERR_DEVICE_CHECK (details in
  * fa_last_error()), or FA_ERR_CUDA if the stream itself reports an error.  */

@@ -31,7 +31,7 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted([
-        "fa_block_mask_build", "fa_block_mask_shape", "fa_fwd", "fa_last_error", "fa_version",
+        "fa_block_mask_build", "fa_block_mask_shape", "fa_fwd", "fa_fwd_noalloc", "fa_last_error", "fa_version",
         "fa_workspace_bytes", "fa_workspace_check"])
 
 
