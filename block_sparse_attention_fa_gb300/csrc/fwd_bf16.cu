@@ -10,7 +10,8 @@
 // Nothing of the T x T matrix ever leaves the SM.
 //
 // Persistent CTAs (two per SM), each taking (b, hq, q-block) work units from a
-// queue in the workspace; 192 threads in four roles:
+// queue in the workspace; 256 threads in four roles (warps 6-7 only hand
+// their registers to the softmax warpgroup):
 //   warps 0-3  softmax: thread r owns query row r (TMEM lane r); reads S from
 //              TMEM (tcgen05.ld), applies score_mod / mask_mod, online max and
 //              sum in base 2, writes P as bf16 back into TMEM over the S
@@ -42,7 +43,13 @@
 namespace fa {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 256;            // warpgroup 0: softmax; warpgroup 1: loader, MMA, 2 idle
+// Registers per thread: launched at 65536 / (2 CTAs x 256) = 128; warpgroup 1
+// gives 88 of them back so that the softmax warpgroup can hold a whole S row:
+// 4 x 32 x 216 + 4 x 32 x 40 = 256 x 128.
+constexpr uint32_t kRegsSoftmax = 216;
+constexpr uint32_t kRegsOther = 40;
+static_assert(kRegsSoftmax * 128 + kRegsOther * 128 == kThreads * 128, "register split must match the launch");
 constexpr uint32_t kTmemCols = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -71,8 +78,9 @@ __device__ __forceinline__ void exp2_poly2(float& p0, float& p1, float a0, float
     ffma2(q0, q1, f0, f1, kExp2C3, kExp2C3, kExp2C2, kExp2C2);
     ffma2(q0, q1, q0, q1, f0, f1, kExp2C1, kExp2C1);
     ffma2(q0, q1, q0, q1, f0, f1, kExp2C0, kExp2C0);
-    p0 = __int_as_float(__float_as_int(q0) + (__float_as_int(t0) << 23));
-    p1 = __int_as_float(__float_as_int(q1) + (__float_as_int(t1) << 23));
+    // q + (round(a) << 23): one integer multiply-add per value
+    p0 = __uint_as_float(__float_as_uint(t0) * (1u << 23) + __float_as_uint(q0));
+    p1 = __uint_as_float(__float_as_uint(t1) * (1u << 23) + __float_as_uint(q1));
 }
 
 // d = a * b on two lanes at once.
@@ -114,6 +122,32 @@ __device__ __forceinline__ void exp_pair(float& p0, float& p1, float x0, float x
     } else {
         p0 = ex2_approx(a0);
         p1 = ex2_approx(a1);
+    }
+}
+
+// P for one row of a tile: p = 2^(x sc - m) as bf16 pairs, with the row sums
+// kept in pairs (rs of the fp32 values, rbs of the bf16-rounded ones).  On a
+// full tile (FULL) the columns with (col % 16) < kPolyCols take the FMA-pipe
+// polynomial; partial tiles (which hold -inf) use MUFU ex2 throughout.
+template <bool FULL>
+__device__ __forceinline__ void exp_row(const float (&x)[128], float sc, float nm, float (&rs)[4],
+                                        float (&rbs)[4], uint32_t (&pk)[2][32]) {
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+            const int col = 64 * c + 2 * e;
+            float p0, p1;
+            if (FULL && (col % 16) < kPolyCols)
+                exp_pair<true>(p0, p1, x[col], x[col + 1], sc, nm);
+            else
+                exp_pair<false>(p0, p1, x[col], x[col + 1], sc, nm);
+            const int a = (e & 1) * 2;
+            fadd2(rs[a], rs[a + 1], rs[a], rs[a + 1], p0, p1);
+            pk[c][e] = pack_bf16x2(p0, p1);
+            fadd2(rbs[a], rbs[a + 1], rbs[a], rbs[a + 1], __uint_as_float(pk[c][e] << 16),
+                  __uint_as_float(pk[c][e] & 0xffff0000u));
+        }
     }
 }
 
@@ -229,6 +263,9 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     // MMA lane and the softmax warps.  Barrier phases run on CTA-wide counters:
     // t counts tiles, nu non-empty units, k taken units.
 
+    if (warp >= 4) {
+    // Warpgroup 1 hands registers to the softmax warpgroup first thing.
+    regs_decrease<kRegsOther>();
     if (warp == 4) {
         // ------------------------------------------------------------ loader
         if (lane == 0) {
@@ -333,8 +370,26 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             mma_commit(bar(B_DRAIN));
             drain_wait(bar(B_DRAIN), 0, wc, S_DRAIN);
         }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+    if (threadIdx.x == 128 && p.ws) {
+        // The last CTA out resets the unit queue, so the workspace is ready
+        // for the next launch on the same stream.
+        __threadfence();
+        if (atomicAdd(p.ws + WS_SCHED_DONE, 1u) == gridDim.x - 1) {
+            atomicExch(p.ws + WS_SCHED_NEXT, 0u);
+            atomicExch(p.ws + WS_SCHED_DONE, 0u);
+            __threadfence();
+        }
+    }
     } else {
         // ----------------------------------------------------------- softmax
+        regs_increase<kRegsSoftmax>();
         const int r = warp * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
         const float sl2 = p.scale * kLog2e;
@@ -376,6 +431,9 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             if (SCORE == FA_SCORE_ALIBI) slope_l2 = p.score.slopes[un.hq] * kLog2e;
             if (SCORE == FA_SCORE_REL_BIAS) rb = p.score.rel_bias + (size_t)un.hq * (2 * p.score.rel_max + 1);
             int kb_next = un.n > 0 ? tile_kb(un, 0) : 0;
+            // this thread's segment id of the next partial tile, loaded a tile ahead
+            int seg_next = (doc && un.n_part > 0 && kb_next * kBlock + r < p.kv_len)
+                               ? __ldg(seg_row + kb_next * kBlock + r) : INT_MAX;
 
             // l: sum of the fp32 probabilities (for lse); lb: sum of the same
             // probabilities rounded to bf16, i.e. of exactly the weights that
@@ -397,8 +455,11 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     const uint32_t ph = doc_tiles & 1;
                     ++doc_tiles;
                     int* buf = seg_tile + ph * 128;
-                    buf[r] = c0 + r < p.kv_len ? __ldg(seg_row + c0 + r) : INT_MAX;
+                    buf[r] = seg_next;
                     mbar_arrive(bar(B_SEG));
+                    if (j + 1 < un.n_part)
+                        seg_next = kb_next * kBlock + r < p.kv_len ? __ldg(seg_row + kb_next * kBlock + r)
+                                                                    : INT_MAX;
                     if (!mbar_wait_warp(bar(B_SEG), ph, wc, S_SEG)) { ok = false; break; }
                     seg_lo = count_below<true>(buf, my_seg);
                     seg_hi = count_below<false>(buf, my_seg) - 1;
@@ -406,12 +467,11 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 if (!mbar_wait_warp(bar(B_S_FULL), t & 1, wc, S_S_FULL)) { ok = false; break; }
                 tc_fence_after();
                 float x[128];
+                {
+                    uint32_t raw[128];
+                    tmem_ld128(tS + lane_off, raw);
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t raw[32];
-                    tmem_ld32(tS + lane_off + 32u * c, raw);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) x[32 * c + e] = __uint_as_float(raw[e]);
+                    for (int e = 0; e < 128; ++e) x[e] = __uint_as_float(raw[e]);
                 }
 
                 // score_mod on every visited element.  Without a score_mod x stays
@@ -536,25 +596,12 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 // bf16-rounded ones.  Full tiles take part of their exponentials on
                 // the FMA pipe; partial tiles (which hold -inf) all on MUFU.
                 float rs[4] = {0.f, 0.f, 0.f, 0.f}, rbs[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int col = 64 * c + 2 * e;
-                        float p0, p1;
-                        if (!partial && (col % 16) < kPolyCols)
-                            exp_pair<true>(p0, p1, x[col], x[col + 1], sc, nm);
-                        else
-                            exp_pair<false>(p0, p1, x[col], x[col + 1], sc, nm);
-                        const int a = (e & 1) * 2;
-                        fadd2(rs[a], rs[a + 1], rs[a], rs[a + 1], p0, p1);
-                        pk[e] = pack_bf16x2(p0, p1);
-                        fadd2(rbs[a], rbs[a + 1], rbs[a], rbs[a + 1], __uint_as_float(pk[e] << 16),
-                              __uint_as_float(pk[e] & 0xffff0000u));
-                    }
-                    tmem_st32(tP + lane_off + 32u * c, pk);
-                }
+                uint32_t pk[2][32];
+                if (partial)
+                    exp_row<false>(x, sc, nm, rs, rbs, pk);
+                else
+                    exp_row<true>(x, sc, nm, rs, rbs, pk);
+                tmem_st64(tP + lane_off, pk[0], pk[1]);
                 l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
                 lb += (rbs[0] + rbs[1]) + (rbs[2] + rbs[3]);
 
@@ -606,23 +653,8 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 p.lse[((size_t)un.b * p.Hq + un.hq) * p.q_len + i] =
                     empty ? -CUDART_INF_F : (m_use + log2f(l)) * kLn2;
         }
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 5) {
-        tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
-    }
-    if (threadIdx.x == 0 && p.ws) {
-        // The last CTA out resets the unit queue, so the workspace is ready
-        // for the next launch on the same stream.
-        __threadfence();
-        if (atomicAdd(p.ws + WS_SCHED_DONE, 1u) == gridDim.x - 1) {
-            atomicExch(p.ws + WS_SCHED_NEXT, 0u);
-            atomicExch(p.ws + WS_SCHED_DONE, 0u);
-            __threadfence();
-        }
+        tc_fence_before();
+        __syncthreads();
     }
 }
 

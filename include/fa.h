@@ -158,9 +158,11 @@ typedef struct fa_fwd_args {
     uint32_t debug_flags;
 } fa_fwd_args;
 
-/* Size in bytes of the device workspace every launching call takes: a few
- * status words.  The caller allocates it once (zero-filled), may reuse it for
- * any number of calls on one device, and reads it with fa_workspace_check(). */
+/* Size in bytes of the device workspace every launching call takes: status
+ * words and the forward's work-queue counters.  The caller allocates it once
+ * (zero-filled) and may reuse it for any number of calls on one device that
+ * run one after another (calls that may run at the same time, on unordered
+ * streams, need separate workspaces); fa_workspace_check() reads it.        */
 size_t fa_workspace_bytes(void);
 
 /* nq and nkv for a (q_len, kv_len) problem, and the element count of each
@@ -189,8 +191,9 @@ fa_status fa_fwd(const fa_fwd_args *a, const fa_block_mask *bm, const fa_score_d
  * that must not call cudaMalloc because it can synchronise the device.  The
  * source pages have no counterpart to this entry point; it is this library's
  * own.  The caller passes inputs and outputs as for fa_fwd, but no workspace:
- * the status words live in a static, 256-byte aligned __device__ array of
- * 4 KiB that every GPU loading the library holds until the process exits.
+ * the status words and the forward's work-queue counters live in a static,
+ * 256-byte aligned __device__ array of 4 KiB that every GPU loading the
+ * library holds until the process exits.
  *   - The first call on a device looks up that array's device address
  *     (cudaGetSymbolAddress, with the device current); make that first call
  *     before any stream capture.
