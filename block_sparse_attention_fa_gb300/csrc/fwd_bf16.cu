@@ -63,8 +63,10 @@ constexpr uint32_t kUnitConsumers = 5;    // the MMA lane + one lane of each sof
 
 // Which columns of a full tile take their exponential on the FMA pipe (the
 // polynomial below) instead of the MUFU ex2 unit: columns with
-// (col % 16) < kPolyCols.  Balances the two pipes.
-constexpr int kPolyCols = 6;
+// (col % 16) < kPolyCols.  Measured on GB300 the softmax is bound by
+// instruction issue, not by MUFU (XU pipe 8-13 % busy), and the polynomial's
+// extra issue slots cost 8-12 % of throughput, so it is off.
+constexpr int kPolyCols = 0;
 
 // 2^a for two values on the FMA pipe, a >= -125: a = n + f with n an integer
 // (rounded by adding 1.5 * 2^23) and f in [-1/2, 1/2]; 2^f by the cubic of
