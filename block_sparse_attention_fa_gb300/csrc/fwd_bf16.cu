@@ -15,8 +15,8 @@
 //   warps 0-3  softmax: thread r owns query row r (TMEM lane r); reads S from
 //              TMEM (tcgen05.ld), applies score_mod / mask_mod, online max and
 //              sum in base 2, writes P as bf16 back into TMEM over the S
-//              columns it has consumed, rescales O in TMEM when the running
-//              max grows by more than 2^8, and runs the epilogue (O / l, lse).
+//              columns it has consumed, rescales O in TMEM whenever the running
+//              max grows, and runs the epilogue (O / l, lse).
 //   warp 4     loader: one lane issues TMA loads of Q (once) and of the K and
 //              V tiles along the index lists.
 //   warp 5     MMA: one lane issues tcgen05.mma: S = Q K^T (A, B from shared
@@ -53,7 +53,6 @@ static_assert(kRegsSoftmax * 128 + kRegsOther * 128 == kThreads * 128, "register
 constexpr uint32_t kTmemCols = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleThreshold = 8.0f;   // base-2 units: O is rescaled when m grows by > 2^8
 
 enum Bar { B_Q_FULL, B_Q_EMPTY, B_K_FULL, B_K_EMPTY, B_V_FULL, B_V_EMPTY, B_S_FULL, B_P_FULL,
            B_O_FULL, B_DRAIN, B_SEG, B_UNIT_FULL, B_UNIT_FULL1, B_UNIT_EMPTY, B_UNIT_EMPTY1, B_COUNT };
@@ -63,9 +62,7 @@ constexpr uint32_t kUnitConsumers = 5;    // the MMA lane + one lane of each sof
 
 // Which columns of a full tile take their exponential on the FMA pipe (the
 // polynomial below) instead of the MUFU ex2 unit: columns with
-// (col % 16) < kPolyCols.  Measured on GB300 the softmax is bound by
-// instruction issue, not by MUFU (XU pipe 8-13 % busy), and the polynomial's
-// extra issue slots cost 8-12 % of throughput, so it is off.
+// (col % 16) < kPolyCols.  Balances the two pipes.
 constexpr int kPolyCols = 0;
 
 // 2^a for two values on the FMA pipe, a >= -125: a = n + f with n an integer
@@ -124,32 +121,6 @@ __device__ __forceinline__ void exp_pair(float& p0, float& p1, float x0, float x
     } else {
         p0 = ex2_approx(a0);
         p1 = ex2_approx(a1);
-    }
-}
-
-// P for one row of a tile: p = 2^(x sc - m) as bf16 pairs, with the row sums
-// kept in pairs (rs of the fp32 values, rbs of the bf16-rounded ones).  On a
-// full tile (FULL) the columns with (col % 16) < kPolyCols take the FMA-pipe
-// polynomial; partial tiles (which hold -inf) use MUFU ex2 throughout.
-template <bool FULL>
-__device__ __forceinline__ void exp_row(const float (&x)[128], float sc, float nm, float (&rs)[4],
-                                        float (&rbs)[4], uint32_t (&pk)[2][32]) {
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-            const int col = 64 * c + 2 * e;
-            float p0, p1;
-            if (FULL && (col % 16) < kPolyCols)
-                exp_pair<true>(p0, p1, x[col], x[col + 1], sc, nm);
-            else
-                exp_pair<false>(p0, p1, x[col], x[col + 1], sc, nm);
-            const int a = (e & 1) * 2;
-            fadd2(rs[a], rs[a + 1], rs[a], rs[a + 1], p0, p1);
-            pk[c][e] = pack_bf16x2(p0, p1);
-            fadd2(rbs[a], rbs[a + 1], rbs[a], rbs[a + 1], __uint_as_float(pk[c][e] << 16),
-                  __uint_as_float(pk[c][e] & 0xffff0000u));
-        }
     }
 }
 
@@ -437,11 +408,10 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             int seg_next = (doc && un.n_part > 0 && kb_next * kBlock + r < p.kv_len)
                                ? __ldg(seg_row + kb_next * kBlock + r) : INT_MAX;
 
-            // l: sum of the fp32 probabilities (for lse); lb: sum of the same
-            // probabilities rounded to bf16, i.e. of exactly the weights that
-            // enter P V, so that O = sum p~ v / sum p~ is a consistent
-            // weighted mean.
-            float m_use = -CUDART_INF_F, l = 0.f, lb = 0.f;
+            // m: the running row max (exact: every increase rescales O and
+            // l, so the row's largest probability is exactly 1 and its bf16
+            // rounding is exact); l: sum of the fp32 probabilities.
+            float m_use = -CUDART_INF_F, l = 0.f;
             for (int j = 0; j < un.n; ++j, ++t) {
                 const bool partial = j < un.n_part;
                 const int kb = kb_next;
@@ -567,52 +537,57 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 }
                 const float mx = fmax3(fmaxf(m4[0], m4[1]), m4[2], m4[3]) * sc;
                 const float m_new = fmaxf(m_use, mx);
-                bool need = false;
-                if (j == 0) {
-                    m_use = m_new;
-                } else {
-                    need = m_new > m_use + kRescaleThreshold;
-                }
-                if (__any_sync(0xffffffffu, need)) {
-                    // O holds the PV products of tiles 0..j-1 (all complete: the S
-                    // commit of tile j tracks every earlier MMA).
-                    const float alpha = need ? ex2_approx(m_use - m_new) : 1.f;
-                    if (need) {
-                        l *= alpha;
-                        lb *= alpha;
-                        m_use = m_new;
-                    }
-#pragma unroll 1
-                    for (int c = 0; c < D / 16; ++c) {
-                        uint32_t o[16];
-                        tmem_ld16(tO + lane_off + 16u * c, o);
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        tmem_st16(tO + lane_off + 16u * c, o);
-                    }
-                }
+                // O and l follow every increase of the max.  O holds the PV
+                // products of tiles 0..j-1 (all complete: the S commit of
+                // tile j tracks every earlier MMA); its rescale is interleaved
+                // with the exponentials below so that the TMEM round trips
+                // overlap arithmetic.
+                const bool need = j > 0 && m_new > m_use;
+                const float alpha = need ? ex2_approx(m_use - m_new) : 1.f;
+                if (need) l *= alpha;
+                m_use = m_new;
+                const bool rescale = __any_sync(0xffffffffu, need);
                 const float nm = m_use == -CUDART_INF_F ? 0.f : -m_use;
 
-                // P = 2^(x sc - m) -> bf16 pairs into TMEM over S; the row sums are
-                // kept in pairs (packed adds): rs of the fp32 values, rb of the
-                // bf16-rounded ones.  Full tiles take part of their exponentials on
-                // the FMA pipe; partial tiles (which hold -inf) all on MUFU.
-                float rs[4] = {0.f, 0.f, 0.f, 0.f}, rbs[4] = {0.f, 0.f, 0.f, 0.f};
-                uint32_t pk[2][32];
-                if (partial)
-                    exp_row<false>(x, sc, nm, rs, rbs, pk);
-                else
-                    exp_row<true>(x, sc, nm, rs, rbs, pk);
-                tmem_st64(tP + lane_off, pk[0], pk[1]);
+                // P = 2^(x sc - m) -> bf16 pairs into TMEM over S, 32 columns
+                // of S (16 of P) at a time.
+                float rs[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t o[32];
+                    const bool oc = rescale && c < D / 32;
+                    if (oc) tmem_ld32_async(tO + lane_off + 32u * c, o);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int col = 32 * c + 2 * e;
+                        float p0, p1;
+                        exp_pair<false>(p0, p1, x[col], x[col + 1], sc, nm);
+                        const int a2 = (e & 1) * 2;
+                        fadd2(rs[a2], rs[a2 + 1], rs[a2], rs[a2 + 1], p0, p1);
+                        pk[e] = pack_bf16x2(p0, p1);
+                    }
+                    if (oc) {
+                        tmem_wait_ld(o);
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            float a0, a1;
+                            fmul2(a0, a1, __uint_as_float(o[e]), __uint_as_float(o[e + 1]), alpha, alpha);
+                            o[e] = __float_as_uint(a0);
+                            o[e + 1] = __float_as_uint(a1);
+                        }
+                        tmem_st32(tO + lane_off + 32u * c, o);
+                    }
+                    tmem_st16(tP + lane_off + 16u * c, pk);
+                }
                 l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
-                lb += (rbs[0] + rbs[1]) + (rbs[2] + rbs[3]);
 
                 tc_fence_before();
                 mbar_arrive(bar(B_P_FULL));
             }
             if (!ok) break;
 
-            // epilogue: O / lb and lse = (m + log2 l) ln 2; a row that saw no
+            // epilogue: O / l and lse = (m + log2 l) ln 2; a row that saw no
             // key gets O = 0 and lse = -inf.
             if (un.n > 0) {
                 if (!mbar_wait_warp(bar(B_O_FULL), nu & 1, wc, S_O_FULL)) break;
@@ -620,7 +595,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 ++nu;
             }
             const bool empty = !(l > 0.f);
-            const float inv = empty ? 0.f : 1.f / lb;
+            const float inv = empty ? 0.f : 1.f / l;
             const bool row_ok = i < p.q_len;
             const bool out32 = (p.flags & FA_OUT_FP32) != 0;
             const size_t row_elem = (((size_t)un.b * p.Hq + un.hq) * p.q_len + i) * D;
