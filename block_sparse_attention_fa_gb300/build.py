@@ -50,6 +50,28 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
+# Kernels that move registers between warpgroups with setmaxnreg: the shares
+# they hand out add up to a fixed per-thread launch count, so the compiled
+# kernel must be launched with exactly that many registers (a smaller launch
+# allocation would leave a setmaxnreg.inc waiting for registers forever).
+LAUNCH_REGISTERS = {"fwd_bf16.cu": ("fwd_bf16_kernel", 128)}
+
+
+def check_launch_registers(src: str, ptxas_log: str) -> None:
+    if src not in LAUNCH_REGISTERS:
+        return
+    kernel, want = LAUNCH_REGISTERS[src]
+    got = []
+    current = None
+    for line in ptxas_log.splitlines():
+        if "Compiling entry function" in line:
+            current = line
+        elif "Used" in line and "registers" in line and current and kernel in current:
+            got.append(int(line.split("Used")[1].split("registers")[0]))
+    if not got or any(g != want for g in got):
+        raise RuntimeError(f"{src}: {kernel} must launch with {want} registers per thread, ptxas reports {got}")
+
+
 def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False) -> str:
     if not force and up_to_date():
         return LIB
@@ -64,10 +86,12 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
 
     def compile_one(src):
         obj = os.path.join(objdir, os.path.basename(src) + ".o")
-        cmd = [nv] + flags + ["-c", src, "-o", obj]
+        extra = ["-Xptxas", "-v"] if os.path.basename(src) in LAUNCH_REGISTERS and not ptxas_verbose else []
+        cmd = [nv] + flags + extra + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{r.stderr}")
+        check_launch_registers(os.path.basename(src), r.stderr)
         if verbose or ptxas_verbose:
             sys.stderr.write(r.stderr)
         return obj

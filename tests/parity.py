@@ -121,6 +121,13 @@ def bf16_half_ulp(x):
     return 2.0 ** (e - 8)
 
 
+def bf16_output_floor(o_ref, o_gpu):
+    """The rounding a bf16 output may add on top of the 2e-2 bound: half a
+    unit at the larger of |O_ref| and |O| (the two can sit on either side of
+    a power of two, where the unit doubles)."""
+    return bf16_half_ulp(np.maximum(np.abs(o_ref), np.abs(o_gpu)))
+
+
 def sample_rows(w, n_random, seed=0, extra_q=()):
     """Flat row indices: n_random seeded random rows over all (b, h, i), plus
     every head's rows i in `extra_q` (q-block edges, the tail)."""

@@ -97,8 +97,9 @@ def test_downscaled_workloads_full_compare(name, small):
         q, k, v = w.qkv()
         o, lse = parity.run_gpu(w, q, k, v, None)
         o_ref, lse_ref = parity.run_oracle(w, q, k, v, None)
-        floor = parity.bf16_half_ulp(o_ref).reshape(-1, w.D)
-        assert np.all(np.abs(o.reshape(-1, w.D) - o_ref.reshape(-1, w.D)) <= parity.BF16_MAX_ABS + floor)
+        o2, r2 = o.reshape(-1, w.D), o_ref.reshape(-1, w.D)
+        excess = np.abs(o2 - r2) - (parity.BF16_MAX_ABS + parity.bf16_output_floor(r2, o2))
+        assert excess.max() <= 0, f"bf16 output over the bound by {excess.max():.3e}"
     else:
         _check_full(w)
 
@@ -129,8 +130,8 @@ def test_causal_softcap_bf16_output_floor():
     o, lse = parity.run_gpu(w, q, k, v, None)
     o_ref, lse_ref = parity.run_oracle(w, q, k, v, None, rows=rows)
     got = o.reshape(-1, w.D)[rows]
-    floor = parity.bf16_half_ulp(o_ref)
-    assert np.all(np.abs(got - o_ref) <= parity.BF16_MAX_ABS + floor)
+    excess = np.abs(got - o_ref) - (parity.BF16_MAX_ABS + parity.bf16_output_floor(o_ref, got))
+    assert excess.max() <= 0, f"bf16 output over the bound by {excess.max():.3e}"
     assert np.linalg.norm(got - o_ref) / np.linalg.norm(o_ref) <= parity.BF16_REL_L2
     np.testing.assert_allclose(lse.reshape(-1)[rows], lse_ref, atol=parity.LSE_TOL["bf16"])
 
@@ -171,3 +172,26 @@ def test_runs_on_a_side_stream():
     s.synchronize()
     o_ref, lse_ref = parity.run_oracle(w, q, k, v, None)
     parity.compare(o.double().cpu().numpy(), o_ref, lse.double().cpu().numpy(), lse_ref, "bf16")
+
+
+@pytest.mark.parametrize("name", ["causal_softcap_bf16", "document_bf16", "grouped_bf16"])
+def test_repeated_launches_are_bitwise_identical(name):
+    """Each row's tiles are reduced in a fixed order, so two launches on the
+    same inputs must agree bit for bit (a race between pipeline roles would
+    show up here as a difference)."""
+    import torch
+    from block_sparse_attention_fa_gb300 import fa
+    w = synth.WORKLOADS[name]
+    q, k, v = w.qkv()
+    seg = w.segments()
+    qd, kd, vd = parity.to_device(w, q, k, v)
+    bm = parity.gpu_block_mask(w, seg)
+    skw = parity.score_kwargs_gpu(w)
+    outs = []
+    for _ in range(3):
+        o, lse = fa.fwd(qd, kd, vd, bm, **skw)
+        outs.append((o.clone(), lse.clone()))
+    fa.default_workspace(qd.device).check()
+    for o, lse in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0][0].view(torch.int16))
+        assert torch.equal(lse, outs[0][1])
