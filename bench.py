@@ -273,6 +273,34 @@ class Runner:
         return sec, h2d, d2h
 
 
+KERNEL_SOURCES = ["fwd_bf16.cu", "fa_api.cu", "ptx.cuh", "fa_internal.h", "exp2_poly.h", "tanh_poly.h"]
+
+
+def kernel_source_digest():
+    """sha256 (first 16 hex digits) of the bf16 forward's sources, in order."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "block_sparse_attention_fa_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload):
+    """DRAM bytes (read + write) of one forward launch from the committed ncu
+    capture of this workload, or None when there is none or the kernel's
+    sources have changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    t = d.get("workloads", {}).get(workload)
+    if t is None or d.get("source_digest") != kernel_source_digest():
+        return None
+    return int(t["read"]) + int(t["write"])
+
+
 def summarize(w, r, step_ms, fwd_ms, peaks, peak_src):
     ms = statistics.median(step_ms)
     fms = statistics.mean(fwd_ms)
@@ -292,6 +320,8 @@ def summarize(w, r, step_ms, fwd_ms, peaks, peak_src):
     else:
         roof = {"bound": "tensor", "achieved": round(fwd_tflops, 1), "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": round(fwd_tflops / peaks["bf16_tflops"], 4), "traffic": None}
+    if w.dtype == "bf16":
+        roof["traffic"] = measured_traffic(w.name)
     roof["peak_source"] = peak_src
     roof["kernel"] = "fwd_bf16_kernel" if w.dtype == "bf16" else "fwd_fp32_kernel"
     roof["kernel_ms"] = round(fms, 4)
