@@ -3,30 +3,38 @@
 // The operation (FlexAttention Guide, "FlexAttention Guide: Custom Fast
 // Attention in PyTorch 2.5", "The Core Design Principles of FlexAttention",
 // items 1-3, and "Systems Mechanics", 1. 128x128 Tile Block Sparsity): for a
-// 128-row query block, visit the kv tiles its BlockMask row lists (partial
-// tiles, then full tiles), compute S = Q K^T on the tensor cores, apply the
-// score_mod to every element and the mask_mod only on partial tiles, keep the
-// online softmax state per row, and accumulate O += P V on the tensor cores.
-// Nothing of the T x T matrix ever leaves the SM.
+// 128-row query block, visit the kv tiles its BlockMask row lists, compute
+// S = Q K^T on the tensor cores, apply the score_mod to every element and the
+// mask_mod only on partial tiles, keep the online softmax state per row, and
+// accumulate O += P V on the tensor cores.  Nothing of the T x T matrix ever
+// leaves the SM.
 //
-// Persistent CTAs (two per SM), each taking (b, hq, q-block) work units from a
-// queue in the workspace; 256 threads in four roles (warps 6-7 only hand
-// their registers to the softmax warpgroup):
-//   warps 0-3  softmax: thread r owns query row r (TMEM lane r); reads S from
-//              TMEM (tcgen05.ld), applies score_mod / mask_mod, online max and
-//              sum in base 2, writes P as bf16 back into TMEM over the S
-//              columns it has consumed, rescales O in TMEM whenever the running
-//              max grows, and runs the epilogue (O / l, lse).
-//   warp 4     loader: one lane issues TMA loads of Q (once) and of the K and
-//              V tiles along the index lists.
-//   warp 5     MMA: one lane issues tcgen05.mma: S = Q K^T (A, B from shared
-//              memory, both K-major) and O += P V (A = P from TMEM, B = V from
-//              shared memory, MN-major); it also owns the TMEM allocation.
-// TMEM (256 columns): S at columns [0, 128) (P packed bf16x2 in [0, 64) once S
-// is consumed), O at [128, 128 + D).  Shared memory holds Q, one K and one V
-// tile (128-byte swizzle, as TMA writes them), so two CTAs fit per SM and the
-// tensor pipe alternates between them: while one CTA runs its softmax the
-// other one's MMAs run.
+// One persistent CTA per SM takes work units from a queue in the workspace.
+// A unit is a PAIR of adjacent 128-row query blocks (2p, 2p + 1) of one
+// (b, hq): the kv tiles of the two BlockMask rows are walked as one ascending
+// sequence (the union of the two rows' partial and full lists), each K/V
+// tile is loaded once and used by whichever of the two query tiles lists it.
+// Every kv tile is processed as two 64-column halves, each with its own S
+// buffer, so that the tensor pipe computes one half's S while the softmax
+// works on the other.  384 threads in five roles:
+//   warps 0-3  softmax of query tile 0, warps 4-7 softmax of query tile 1:
+//              thread r of the warpgroup owns row r (TMEM lane r).  For each
+//              half it reads its row of S (tcgen05.ld), applies score_mod /
+//              mask_mod, keeps the running max and sum in base 2, writes P as
+//              bf16 into TMEM over the S columns it has read, rescales its row
+//              of O whenever the max grows, and at the end of the unit runs
+//              the epilogue (O / l, lse).
+//   warp 8     loader: one lane issues TMA loads of the two Q tiles and of the
+//              K and V tiles along the sequence into a STAGES-deep ring (K one
+//              step ahead of V).
+//   warps 9-10 MMA, one warp per query tile t: O_t += P_t,h V(k), then
+//              S_t,h = Q_t K(k+1) into the buffer that product released.  The
+//              two warps issue independently (one elected lane each), so each
+//              tile's S comes back as soon as its P is ready.
+//   warp 11    hands its registers to the softmax warpgroups.
+// TMEM (512 columns): S_t,h (64 columns) at 128 t + 64 h, O_t at 256 + D t;
+// P_t,h is packed bf16x2 into the first 32 columns of S_t,h once S_t,h has
+// been read.
 //
 // Every wait is bounded (ptx.cuh): on timeout the CTA records the site in the
 // workspace, the roles leave their loops, outstanding copies and MMAs are
@@ -43,26 +51,45 @@
 namespace fa {
 namespace {
 
-constexpr int kThreads = 256;            // warpgroup 0: softmax; warpgroup 1: loader, MMA, 2 idle
-// Registers per thread: launched at 65536 / (2 CTAs x 256) = 128; warpgroup 1
-// gives 88 of them back so that the softmax warpgroup can hold a whole S row:
-// 4 x 32 x 216 + 4 x 32 x 40 = 256 x 128.
-constexpr uint32_t kRegsSoftmax = 216;
-constexpr uint32_t kRegsOther = 40;
-static_assert(kRegsSoftmax * 128 + kRegsOther * 128 == kThreads * 128, "register split must match the launch");
-constexpr uint32_t kTmemCols = 256;
+constexpr int kThreads = 384;   // warpgroups 0-1: softmax; warpgroup 2: loader, 2 MMA, 1 idle
+// Registers per thread: one CTA per SM is launched with 168 (65536 / 384,
+// rounded down to 8); warpgroup 2 gives 48 of them to the two softmax
+// warpgroups: 4 x 32 x (192 + 192 + 120) = 384 x 168.  build.py checks the
+// launch count.
+constexpr uint32_t kRegsLaunch = 168;
+constexpr uint32_t kRegsSoftmax = 192;
+constexpr uint32_t kRegsOther = 120;
+static_assert(128 * (2 * kRegsSoftmax + kRegsOther) == kThreads * kRegsLaunch,
+              "register split must match the launch");
+constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kMaxStages = 4;
 
-enum Bar { B_Q_FULL, B_Q_EMPTY, B_K_FULL, B_K_EMPTY, B_V_FULL, B_V_EMPTY, B_S_FULL, B_P_FULL,
-           B_O_FULL, B_DRAIN, B_SEG, B_UNIT_FULL, B_UNIT_FULL1, B_UNIT_EMPTY, B_UNIT_EMPTY1, B_COUNT };
+// Barriers (mbarrier indices); B_X + t is the barrier of query tile t, B_X + s
+// that of ring stage s.
+enum Bar {
+    B_Q_FULL = 0, B_Q_EMPTY = 2,
+    B_K_FULL = 4, B_K_EMPTY = B_K_FULL + kMaxStages,
+    B_V_FULL = B_K_EMPTY + kMaxStages, B_V_EMPTY = B_V_FULL + kMaxStages,
+    B_S_FULL = B_V_EMPTY + kMaxStages,          // four (2 t + h): MMA commit of S_t,h
+    B_P_FULL = B_S_FULL + 4,                    // four (2 t + h): 128 softmax threads of tile t
+    B_O_DONE = B_P_FULL + 4,                    // two: MMA commit after a unit's last P_t V
+    B_O_UPD = B_O_DONE + 2,                     // two: MMA commit after every P_t V
+    B_SEG = B_O_UPD + 2,                        // two: 128 softmax threads, per document tile
+    B_UNIT_FULL = B_SEG + 2,                    // two slots
+    B_UNIT_EMPTY = B_UNIT_FULL + 2,             // two slots
+    B_DRAIN = B_UNIT_EMPTY + 2,                 // two: one per MMA warp
+    B_COUNT = B_DRAIN + 2
+};
 enum Site : uint32_t { S_Q = 1, S_Q_EMPTY, S_K_FULL, S_K_EMPTY, S_V_FULL, S_V_EMPTY, S_S_FULL,
-                       S_P_FULL, S_O_FULL, S_DRAIN, S_LOAD_DRAIN, S_SEG, S_UNIT_FULL, S_UNIT_EMPTY };
-constexpr uint32_t kUnitConsumers = 5;    // the MMA lane + one lane of each softmax warp
+                       S_P_FULL, S_O_DONE, S_DRAIN, S_LOAD_DRAIN, S_SEG, S_UNIT_FULL, S_UNIT_EMPTY,
+                       S_O_UPD };
+constexpr uint32_t kUnitConsumers = 10;   // one lane of each MMA warp and of each softmax warp
 
 // Which columns of a full tile take their exponential on the FMA pipe (the
 // polynomial below) instead of the MUFU ex2 unit: columns with
-// (col % 16) < kPolyCols.  Balances the two pipes.
+// (col % 16) < kPolyCols.  0 = all on MUFU.
 constexpr int kPolyCols = 0;
 
 // 2^a for two values on the FMA pipe, a >= -125: a = n + f with n an integer
@@ -126,19 +153,21 @@ __device__ __forceinline__ void exp_pair(float& p0, float& p1, float x0, float x
 
 template <int D>
 struct Layout {
+    static constexpr int kStages = D == 64 ? 4 : 2;       // K/V ring depth
     static constexpr uint32_t kTile = 128u * D * 2u;      // one 128 x D bf16 tile
-    static constexpr uint32_t kQ = 0;
-    static constexpr uint32_t kK = kQ + kTile;
-    static constexpr uint32_t kV = kK + kTile;
-    static constexpr uint32_t kBars = kV + kTile;
+    static constexpr uint32_t kQ = 0;                     // Q0, Q1
+    static constexpr uint32_t kK = kQ + 2 * kTile;        // kStages K tiles
+    static constexpr uint32_t kV = kK + kStages * kTile;  // kStages V tiles
+    static constexpr uint32_t kBars = kV + kStages * kTile;
     static constexpr uint32_t kTmemSlot = kBars + 8 * B_COUNT;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
-    static constexpr uint32_t kUnitQ = kAbort + 4;        // 2 x int32: the unit queue
-    static constexpr uint32_t kSegTile = kUnitQ + 8;      // 2 x 128 int32 (document masks)
-    static constexpr uint32_t kUsed = kSegTile + 2 * 128 * 4;
-    // +1 KB for aligning the base to the 1024-byte swizzle atom; at least
-    // 80 KB so that no more than two CTAs (2 x 256 TMEM columns) share an SM.
-    static constexpr uint32_t kDynamic = (kUsed + 1024 > 80u * 1024u) ? kUsed + 1024 : 80u * 1024u;
+    static constexpr uint32_t kUnitQ = kAbort + 4;        // 2 slots x (unit, has steps)
+    static constexpr uint32_t kStepFlags = kUnitQ + 16;   // kStages x uint32: flags of each stage's step
+    static constexpr uint32_t kSegTile = (kStepFlags + 4 * kMaxStages + 15) & ~15u;  // [2 tiles][2][128] int32
+    static constexpr uint32_t kUsed = kSegTile + 2 * 2 * 128 * 4;
+    static constexpr uint32_t kDynamic = kUsed + 1024;    // + 1 KB to align the base to 1024
+    static_assert(kDynamic <= 227u * 1024u, "shared memory budget");
+    static_assert(kStages <= kMaxStages, "too many stages");
 };
 
 // A drain wait: bounded by time only (it must not be cut short by the abort
@@ -156,68 +185,132 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, const 
     }
 }
 
-// A work unit: one (b, hq, 128-row q-block) and its BlockMask row.
-struct Unit {
-    int b, hq, hkv, qb;
-    int n_part, n;
-    const int32_t* part_idx;
-    const int32_t* full_idx;
+// A work unit: one (b, hq) and the pair of query blocks 2 pr, 2 pr + 1.
+struct Pair {
+    int b, hq, hkv, pr;
 };
 
-// Unit order: (b, kv head) outer, q-blocks from the last (the longest under
-// causal masks) to the first, the query heads of a GQA group innermost, so
-// that units handed out together share K/V tiles in L2.
-__device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
-    Unit x;
+// Unit order: (b, kv head) outer, query-block pairs from the last (the
+// longest under causal masks) to the first, the query heads of a GQA group
+// innermost, so that units handed out together share K/V tiles in L2.
+__device__ __forceinline__ Pair decode_pair(const FwdParams& p, int u) {
+    const int np = (p.bm.nq + 1) >> 1;
+    Pair x;
     int idx = u;
     const int g = idx % p.group;
     idx /= p.group;
-    x.qb = p.bm.nq - 1 - (idx % p.bm.nq);
-    idx /= p.bm.nq;
+    x.pr = np - 1 - (idx % np);
+    idx /= np;
     x.hkv = idx % p.Hkv;
     x.b = idx / p.Hkv;
     x.hq = x.hkv * p.group + g;
-    const int mb = p.bm.B == 1 ? 0 : x.b, mh = p.bm.H == 1 ? 0 : x.hq;
-    const size_t mrow = ((size_t)mb * p.bm.H + mh) * p.bm.nq + x.qb;
-    x.n_part = p.bm.kv_num_blocks[mrow];
-    x.n = x.n_part + p.bm.full_kv_num_blocks[mrow];
-    x.part_idx = p.bm.kv_indices + mrow * p.bm.nkv;
-    x.full_idx = p.bm.full_kv_indices + mrow * p.bm.nkv;
     return x;
 }
 
-__device__ __forceinline__ int tile_kb(const Unit& x, int j) {
-    return j < x.n_part ? x.part_idx[j] : x.full_idx[j - x.n_part];
-}
+// The kv tiles of one BlockMask row in ascending order: the row's partial
+// and full lists (each ascending, disjoint) merged as they are walked.  The
+// next entry of a list is loaded when its head is taken, a whole step before
+// it is compared.  A query block past the last one has no tiles.
+struct RowSeq {
+    const int32_t* part;
+    const int32_t* full;
+    int n_part, n_full, ip, jf;
+    int hp, hf;    // heads: next partial / full kv block, INT_MAX when done
+
+    __device__ __forceinline__ void init(const FwdParams& p, int b, int hq, int qb) {
+        ip = jf = 0;
+        n_part = n_full = 0;
+        part = full = nullptr;
+        hp = hf = INT_MAX;
+        if (qb >= p.bm.nq) return;
+        const int mb = p.bm.B == 1 ? 0 : b, mh = p.bm.H == 1 ? 0 : hq;
+        const size_t mrow = ((size_t)mb * p.bm.H + mh) * p.bm.nq + qb;
+        n_part = __ldg(p.bm.kv_num_blocks + mrow);
+        n_full = __ldg(p.bm.full_kv_num_blocks + mrow);
+        part = p.bm.kv_indices + mrow * p.bm.nkv;
+        full = p.bm.full_kv_indices + mrow * p.bm.nkv;
+        if (n_part > 0) hp = __ldg(part);
+        if (n_full > 0) hf = __ldg(full);
+    }
+    // (by the counts, so that it never waits for the head just requested)
+    __device__ __forceinline__ bool empty() const { return ip >= n_part && jf >= n_full; }
+    __device__ __forceinline__ int head() const { return min(hp, hf); }
+    // Takes the head; returns whether it was a partial tile.
+    __device__ __forceinline__ bool pop() {
+        if (hp < hf) {
+            ++ip;
+            hp = ip < n_part ? __ldg(part + ip) : INT_MAX;
+            return true;
+        }
+        ++jf;
+        hf = jf < n_full ? __ldg(full + jf) : INT_MAX;
+        return false;
+    }
+};
+
+// Flags of one step of a pair's sequence.
+constexpr uint32_t kInTile0 = 1u;         // << t: query tile t visits the step's kv block
+constexpr uint32_t kLastOfTile0 = 4u;     // << t: and it is tile t's last of the unit
+constexpr uint32_t kLastOfUnit = 16u;     // no step follows in this unit
+
+// The pair's sequence: the union of the two rows' tiles, ascending.  Each
+// step names one kv block and, in its flags, which of the two query tiles
+// visit it.
+struct PairSeq {
+    RowSeq row[2];
+    __device__ __forceinline__ void init(const FwdParams& p, const Pair& u) {
+        row[0].init(p, u.b, u.hq, 2 * u.pr);
+        row[1].init(p, u.b, u.hq, 2 * u.pr + 1);
+    }
+    __device__ __forceinline__ bool empty() const { return row[0].empty() && row[1].empty(); }
+    __device__ __forceinline__ bool next(int& kb, uint32_t& flags) {
+        if (empty()) return false;
+        kb = min(row[0].head(), row[1].head());
+        flags = 0;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            if (row[t].head() != kb) continue;
+            row[t].pop();
+            flags |= kInTile0 << t;
+            if (row[t].empty()) flags |= kLastOfTile0 << t;
+        }
+        if (empty()) flags |= kLastOfUnit;
+        return true;
+    }
+};
 
 template <int D, int SCORE>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
 fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
     using L = Layout<D>;
+    constexpr int ST = L::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_addr(smem);
-    const uint32_t sQ = sbase + L::kQ, sK = sbase + L::kK, sV = sbase + L::kV;
     auto bar = [&](int k) { return sbase + L::kBars + 8u * k; };
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + L::kTmemSlot);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
     volatile int* unit_q = reinterpret_cast<volatile int*>(smem + L::kUnitQ);
+    volatile uint32_t* step_flags = reinterpret_cast<volatile uint32_t*>(smem + L::kStepFlags);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
         for (int k = 0; k < B_COUNT; ++k) {
             uint32_t cnt = 1;
-            if (k == B_P_FULL || k == B_SEG) cnt = 128;
-            if (k == B_UNIT_EMPTY || k == B_UNIT_EMPTY1) cnt = kUnitConsumers;
+            if ((k >= B_P_FULL && k < B_P_FULL + 4) || k == B_SEG || k == B_SEG + 1) cnt = 128;
+            if (k == B_UNIT_EMPTY || k == B_UNIT_EMPTY + 1) cnt = kUnitConsumers;
+            // a stage is free once both MMA warps have released it
+            if (k >= B_K_EMPTY && k < B_K_EMPTY + kMaxStages) cnt = 2;
+            if (k >= B_V_EMPTY && k < B_V_EMPTY + kMaxStages) cnt = 2;
             mbar_init(bar(k), cnt);
         }
         *abort_flag = 0;
         mbar_fence_init();
     }
-    if (warp == 5) {
+    if (warp == 9) {
         tmem_alloc(smem_addr(const_cast<uint32_t*>(tmem_slot)), kTmemCols);
         tmem_relinquish();
     }
@@ -225,28 +318,26 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tS = tmem;          // S: columns [0, 128)
-    const uint32_t tP = tmem;          // P (bf16x2): columns [0, 64), written after S is read
-    const uint32_t tO = tmem + 128;    // O: columns [128, 128 + D)
     const WaitCtl wc{abort_flag, p.ws, p.timeout_ns};
 
-    // Persistent CTA: units come from a queue in the workspace (one atomic
-    // counter, handed out in the order of decode_unit).  The loader lane takes
-    // them and passes each through a two-slot queue in shared memory to the
-    // MMA lane and the softmax warps.  Barrier phases run on CTA-wide counters:
-    // t counts tiles, nu non-empty units, k taken units.
+    // Units come from a queue in the workspace (one atomic counter, handed
+    // out in the order of decode_pair).  The loader lane takes them and passes
+    // each through a two-slot queue in shared memory to the MMA lane and the
+    // softmax warps.  Barrier phases run on counters every role keeps alike:
+    // g counts steps (ring stage g % ST), uq[t] units in which query tile t
+    // visits something (Q buffer t), n[t] the steps of tile t.
 
-    if (warp >= 4) {
-    // Warpgroup 1 hands registers to the softmax warpgroup first thing.
+    if (warp >= 8) {
+    // Warpgroup 2 hands registers to the softmax warpgroups first thing.
     regs_decrease<kRegsOther>();
-    if (warp == 4) {
+    if (warp == 8) {
         // ------------------------------------------------------------ loader
         if (lane == 0) {
             tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
-            uint32_t k = 0, t = 0, nu = 0;
-            int last_q = -1, last_k = -1, last_v = -1;
+            uint32_t k = 0, g = 0, uq[2] = {0u, 0u};
+            int last_q[2] = {-1, -1}, last_k = -1, last_v = -1;
             bool ok = true;
             while (ok) {
                 const uint32_t slot = k & 1;
@@ -254,103 +345,237 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     break;
                 int u = static_cast<int>(atomicAdd(p.ws + WS_SCHED_NEXT, 1u));
                 if (u >= p.num_units) u = -1;
-                unit_q[slot] = u;
+                Pair pu{};
+                PairSeq seq;
+                if (u >= 0) {
+                    pu = decode_pair(p, u);
+                    seq.init(p, pu);
+                }
+                unit_q[2 * slot] = u;
+                unit_q[2 * slot + 1] = u >= 0 && !seq.empty();
                 mbar_arrive(bar(B_UNIT_FULL + slot));
                 ++k;
                 if (u < 0) break;
-                const Unit un = decode_unit(p, u);
-                if (un.n == 0) continue;
-                if (nu > 0 && !mbar_wait(bar(B_Q_EMPTY), (nu - 1) & 1, wc, S_Q_EMPTY)) break;
-                mbar_arrive_expect_tx(bar(B_Q_FULL), L::kTile);
+                // the Q tile of each query block that visits anything
 #pragma unroll
-                for (int c = 0; c < D / 64; ++c)
-                    tma_load_4d(sQ + c * 16384u, &tmQ, bar(B_Q_FULL), c * 64, un.qb * kBlock, un.hq, un.b);
-                last_q = static_cast<int>(nu);
-                for (int j = 0; j < un.n; ++j, ++t) {
-                    const int kb = tile_kb(un, j);
-                    if (t > 0 && !mbar_wait(bar(B_K_EMPTY), (t - 1) & 1, wc, S_K_EMPTY)) { ok = false; break; }
-                    if (!((p.debug_flags & FA_DEBUG_DROP_FIRST_LOAD) && t == 0)) {
-                        mbar_arrive_expect_tx(bar(B_K_FULL), L::kTile);
-#pragma unroll
-                        for (int c = 0; c < D / 64; ++c)
-                            tma_load_4d(sK + c * 16384u, &tmK, bar(B_K_FULL), c * 64, kb * kBlock, un.hkv, un.b);
-                        last_k = static_cast<int>(t);
+                for (int t = 0; t < 2; ++t) {
+                    if (seq.row[t].empty()) continue;
+                    if (uq[t] > 0 && !mbar_wait(bar(B_Q_EMPTY + t), (uq[t] - 1) & 1, wc, S_Q_EMPTY)) {
+                        ok = false;
+                        break;
                     }
-                    if (t > 0 && !mbar_wait(bar(B_V_EMPTY), (t - 1) & 1, wc, S_V_EMPTY)) { ok = false; break; }
-                    mbar_arrive_expect_tx(bar(B_V_FULL), L::kTile);
+                    mbar_arrive_expect_tx(bar(B_Q_FULL + t), L::kTile);
 #pragma unroll
                     for (int c = 0; c < D / 64; ++c)
-                        tma_load_4d(sV + c * 16384u, &tmV, bar(B_V_FULL), c * 64, kb * kBlock, un.hkv, un.b);
-                    last_v = static_cast<int>(t);
+                        tma_load_4d(sbase + L::kQ + t * L::kTile + c * 16384u, &tmQ, bar(B_Q_FULL + t), c * 64,
+                                    (2 * pu.pr + t) * kBlock, pu.hq, pu.b);
+                    last_q[t] = static_cast<int>(uq[t]);
+                    ++uq[t];
                 }
-                ++nu;
+                // K runs one step ahead of V inside a unit: S = Q K^T of a
+                // step is issued during the previous step's P V, so K(g) goes
+                // out before V(g - 1).
+                auto load_v = [&](uint32_t gv, int kbv) -> bool {
+                    const uint32_t sv = gv % ST;
+                    if (gv >= ST && !mbar_wait(bar(B_V_EMPTY + sv), (gv / ST - 1) & 1, wc, S_V_EMPTY))
+                        return false;
+                    mbar_arrive_expect_tx(bar(B_V_FULL + sv), L::kTile);
+#pragma unroll
+                    for (int c = 0; c < D / 64; ++c)
+                        tma_load_4d(sbase + L::kV + sv * L::kTile + c * 16384u, &tmV, bar(B_V_FULL + sv),
+                                    c * 64, kbv * kBlock, pu.hkv, pu.b);
+                    last_v = static_cast<int>(gv);
+                    return true;
+                };
+                int kb, kb_pend = -1;
+                uint32_t flags;
+                while (ok && seq.next(kb, flags)) {
+                    const uint32_t s = g % ST;
+                    if (g >= ST && !mbar_wait(bar(B_K_EMPTY + s), (g / ST - 1) & 1, wc, S_K_EMPTY)) {
+                        ok = false;
+                        break;
+                    }
+                    // the MMA warp reads them after K_FULL (whose arrival
+                    // below releases this store) and before K_EMPTY
+                    step_flags[s] = flags;
+                    if (!((p.debug_flags & FA_DEBUG_DROP_FIRST_LOAD) && g == 0)) {
+                        mbar_arrive_expect_tx(bar(B_K_FULL + s), L::kTile);
+#pragma unroll
+                        for (int c = 0; c < D / 64; ++c)
+                            tma_load_4d(sbase + L::kK + s * L::kTile + c * 16384u, &tmK, bar(B_K_FULL + s),
+                                        c * 64, kb * kBlock, pu.hkv, pu.b);
+                        last_k = static_cast<int>(g);
+                    }
+                    if (kb_pend >= 0 && !load_v(g - 1, kb_pend)) { ok = false; break; }
+                    kb_pend = kb;
+                    ++g;
+                }
+                if (ok && kb_pend >= 0 && !load_v(g - 1, kb_pend)) ok = false;
             }
-            // Let every issued copy land before the CTA may exit.
-            if (last_q >= 0) drain_wait(bar(B_Q_FULL), last_q & 1, wc, S_LOAD_DRAIN);
-            if (last_k >= 0) drain_wait(bar(B_K_FULL), last_k & 1, wc, S_LOAD_DRAIN);
-            if (last_v >= 0) drain_wait(bar(B_V_FULL), last_v & 1, wc, S_LOAD_DRAIN);
+            // Let every issued copy land before the CTA may exit: the last
+            // load into each Q buffer and each stage (last_k skips a K load
+            // that the debug flag dropped).
+#pragma unroll
+            for (int t = 0; t < 2; ++t)
+                if (last_q[t] >= 0) drain_wait(bar(B_Q_FULL + t), last_q[t] & 1, wc, S_LOAD_DRAIN);
+            for (int s = 0; s < ST; ++s) {
+                const int lk = last_k - (((last_k - s) % ST + ST) % ST);
+                if (lk >= 0) drain_wait(bar(B_K_FULL + s), (lk / ST) & 1, wc, S_LOAD_DRAIN);
+                const int lv = last_v - (((last_v - s) % ST + ST) % ST);
+                if (lv >= 0) drain_wait(bar(B_V_FULL + s), (lv / ST) & 1, wc, S_LOAD_DRAIN);
+            }
         }
-    } else if (warp == 5) {
+    } else if (warp == 9 || warp == 10) {
         // --------------------------------------------------------------- MMA
-        if (lane == 0) {
-            constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false);
+        // Warp 9 issues the products of query tile 0, warp 10 those of tile
+        // 1, so that each tile's S comes back as soon as its P is released
+        // whatever the other tile is doing; the tensor pipe interleaves the
+        // two streams.  Each warp walks every step of the unit (to keep the
+        // ring's phases) and releases each stage once (K_EMPTY and V_EMPTY
+        // count the two warps).  The whole warp runs the loop, so that every
+        // descriptor is warp-uniform; one elected lane issues each tcgen05
+        // instruction.
+        const int t = warp - 9;
+        {
+            constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 64, false);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
-            uint32_t k = 0, t = 0, nu = 0;
+            // Descriptors of the operand tiles at their first K step; a K
+            // step moves the start address (bits 0-13, in 16-byte units) by a
+            // constant.  Q_t: K-major; K and V stage s: 8 KB per 64 rows.
+            const uint64_t q_desc = sdesc_sw128(sbase + L::kQ + t * L::kTile, 16, 1024);
+            const uint64_t k_desc0 = sdesc_sw128(sbase + L::kK, 16, 1024);
+            const uint64_t v_desc0 = sdesc_sw128(sbase + L::kV, 16384, 1024);
+            const uint32_t tSt = tmem + 128u * t, tOt = tmem + 256u + D * t;
+            // S_t,h = Q_t K(step gg, rows 64 h .. 64 h + 63)^T: N = 64, K = D in
+            // steps of 16 (32 bytes inside the 128-byte swizzled row; the next
+            // 64-column block 16 KB on).
+            auto issue_qk = [&](int h, uint32_t gg) {
+                const uint64_t kd = k_desc0 + (((gg % ST) * L::kTile + 8192u * h) >> 4);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = ((kk >> 2) * 16384u + (kk & 3) * 32u) >> 4;
+                    mma_ss_elect(tSt + 64u * h, q_desc + off, kd + off, idesc_qk, kk > 0);
+                }
+                mma_commit_elect(bar(B_S_FULL + 2 * t + h));
+            };
+            // O_t += P_t,h V(step gg, rows 64 h .. 64 h + 63): K = 64 kv rows in
+            // steps of 16 (16 rows x 128 B = 2 KB of V); P's 16 bf16 per step
+            // = 8 TMEM columns.  V is MN-major: 64-column blocks 16 KB apart
+            // (LBO), 8-row groups 1 KB apart (SBO).  A unit's first product
+            // overwrites O_t (its softmax read the previous unit's O_t before
+            // releasing this P_t,0).
+            auto issue_pv = [&](int h, uint32_t gg, bool accumulate) {
+                const uint64_t vd = v_desc0 + (((gg % ST) * L::kTile + 8192u * h) >> 4);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_ts_elect(tOt, tSt + 64u * h + kk * 8u, vd + kk * 128u, idesc_pv,
+                                 (accumulate || kk > 0) ? 1u : 0u);
+                mma_commit_elect(bar(B_O_UPD + t));
+            };
+            const uint32_t in_t = kInTile0 << t, last_t = kLastOfTile0 << t;
+            // np: steps of tile t whose P has been consumed (the phase of both
+            // P_FULL_t,h barriers); uq: units in which tile t took part
+            uint32_t k = 0, g = 0, uq = 0, np = 0;
             bool ok = true;
             while (ok) {
                 const uint32_t slot = k & 1;
-                if (!mbar_wait(bar(B_UNIT_FULL + slot), (k >> 1) & 1, wc, S_UNIT_FULL)) break;
-                const int u = unit_q[slot];
-                mbar_arrive(bar(B_UNIT_EMPTY + slot));
+                if (!mbar_wait_warp(bar(B_UNIT_FULL + slot), (k >> 1) & 1, wc, S_UNIT_FULL)) break;
+                const int u = unit_q[2 * slot];
+                const bool has_steps = unit_q[2 * slot + 1] != 0;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_UNIT_EMPTY + slot));
                 ++k;
                 if (u < 0) break;
-                const Unit un = decode_unit(p, u);
-                if (un.n == 0) continue;
-                if (!mbar_wait(bar(B_Q_FULL), nu & 1, wc, S_Q)) break;
-                for (int j = 0; j < un.n; ++j, ++t) {
-                    if (!mbar_wait(bar(B_K_FULL), t & 1, wc, S_K_FULL)) { ok = false; break; }
+                if (!has_steps) continue;
+                bool q_ready = false, started = false;
+                // Q_t is waited for at the tile's first product of the unit
+                auto need_q = [&]() -> bool {
+                    if (q_ready) return true;
+                    if (!mbar_wait_warp(bar(B_Q_FULL + t), uq & 1, wc, S_Q)) return false;
+                    q_ready = true;
+                    return true;
+                };
+                // the first step's products, both halves; each step's flags
+                // come with its K
+                if (!mbar_wait_warp(bar(B_K_FULL + g % ST), (g / ST) & 1, wc, S_K_FULL)) break;
+                uint32_t f = step_flags[g % ST];
+                tc_fence_after();
+                if (f & in_t) {
+                    if (!need_q()) break;
                     tc_fence_after();
-                    // S = Q K^T: K = D in steps of 16 (32 bytes inside the
-                    // 128-byte swizzled row; next 64-column block +16 KB).
+                    issue_qk(0, g);
+                    issue_qk(1, g);
+                    if (f & last_t) mma_commit_elect(bar(B_Q_EMPTY + t));
+                }
+                mma_commit_elect(bar(B_K_EMPTY + g % ST));
+                // Step g: for each half h, O_t += P_t,h V(g) and then, into the
+                // S buffer that product has just released, S_t,h = Q_t K(g + 1)
+                // for the next step.
+                while (true) {
+                    const bool more = !(f & kLastOfUnit);
+                    const uint32_t g1 = g + 1;
+                    uint32_t fn = 0;
+                    bool k_ready = !more;
+                    auto need_k = [&]() -> bool {
+                        if (k_ready) return true;
+                        if (!mbar_wait_warp(bar(B_K_FULL + g1 % ST), (g1 / ST) & 1, wc, S_K_FULL)) return false;
+                        fn = step_flags[g1 % ST];
+                        k_ready = true;
+                        return true;
+                    };
+                    // Both warps wait for V(g) (and for K of every step), even
+                    // where their tile does not visit the step: a stage's
+                    // barrier phase then completes before either warp can
+                    // arrive on the stage's next phase.
+                    if (!mbar_wait_warp(bar(B_V_FULL + g % ST), (g / ST) & 1, wc, S_V_FULL)) { ok = false; break; }
+                    if (f & in_t) {
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * 16384u + (kk & 3) * 32u;
-                        mma_ss(tS, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024),
-                               idesc_qk, kk > 0);
+                        for (int h = 0; h < 2; ++h) {
+                            if (!mbar_wait_warp(bar(B_P_FULL + 2 * t + h), np & 1, wc, S_P_FULL)) { ok = false; break; }
+                            tc_fence_after();
+                            issue_pv(h, g, started);
+                            started = true;
+                            if (!need_k()) { ok = false; break; }
+                            if (fn & in_t) {
+                                if (!need_q()) { ok = false; break; }
+                                tc_fence_after();
+                                issue_qk(h, g1);
+                            }
+                        }
+                        if (!ok) break;
+                        ++np;
+                        if (f & last_t) mma_commit_elect(bar(B_O_DONE + t));
+                    } else {
+                        if (!need_k()) { ok = false; break; }
+                        if (fn & in_t) {
+                            if (!need_q()) { ok = false; break; }
+                            tc_fence_after();
+                            issue_qk(0, g1);
+                            issue_qk(1, g1);
+                        }
                     }
-                    mma_commit(bar(B_S_FULL));
-                    mma_commit(bar(B_K_EMPTY));
-                    if (j == un.n - 1) mma_commit(bar(B_Q_EMPTY));
-                    if (!mbar_wait(bar(B_P_FULL), t & 1, wc, S_P_FULL)) { ok = false; break; }
-                    if (!mbar_wait(bar(B_V_FULL), t & 1, wc, S_V_FULL)) { ok = false; break; }
-                    tc_fence_after();
-                    // O += P V: K = 128 kv rows in steps of 16 (16 rows x 128 B
-                    // = 2 KB of V); P's 16 bf16 per step = 8 TMEM columns.
-                    // V is MN-major: 64-column blocks 16 KB apart (LBO), 8-row
-                    // groups 1 KB apart (SBO).  The first step of a unit
-                    // overwrites O (the softmax warps read the previous unit's
-                    // O before they released this unit's first P).
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_ts(tO, tP + kk * 8u, sdesc_sw128(sV + kk * 2048u, 16384, 1024), idesc_pv,
-                               (j > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(bar(B_V_EMPTY));
+                    if (more && (fn & last_t)) mma_commit_elect(bar(B_Q_EMPTY + t));
+                    mma_commit_elect(bar(B_V_EMPTY + g % ST));
+                    if (more) mma_commit_elect(bar(B_K_EMPTY + g1 % ST));
+                    g = g1;
+                    if (!more) break;
+                    f = fn;
                 }
                 if (!ok) break;
-                mma_commit(bar(B_O_FULL));
-                ++nu;
+                if (q_ready) ++uq;
             }
-            mma_commit(bar(B_DRAIN));
-            drain_wait(bar(B_DRAIN), 0, wc, S_DRAIN);
+            mma_commit_elect(bar(B_DRAIN + t));
+            drain_wait(bar(B_DRAIN + t), 0, wc, S_DRAIN);
+            __syncwarp();
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
-    if (threadIdx.x == 128 && p.ws) {
+    if (threadIdx.x == 256 && p.ws) {
         // The last CTA out resets the unit queue, so the workspace is ready
         // for the next launch on the same stream.
         __threadfence();
@@ -363,15 +588,20 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     } else {
         // ----------------------------------------------------------- softmax
         regs_increase<kRegsSoftmax>();
-        const int r = warp * 32 + lane;
-        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const int t = warp >> 2;                    // query tile of this warpgroup
+        const int wq = warp & 3;                    // its 32 rows: TMEM lanes 32 wq ..
+        const int r = wq * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+        const uint32_t tS = tmem + 128u * t;        // S_t; P_t (bf16x2) in its first 64 columns
+        const uint32_t tP = tS;
+        const uint32_t tO = tmem + 256u + D * t;
         const float sl2 = p.scale * kLog2e;
         const bool doc = p.mask.kind == FA_MASK_DOCUMENT;
-        float cap_in = 0.f, cap_out = 0.f, s2_lim = 0.f;
+        float cap_in = 0.f, cap_out = 0.f, s_lim = 0.f;
         float tq0 = 0.f, tq1 = 0.f, tq2 = 0.f, tq3 = 0.f, tq4 = 0.f;
         if (SCORE == FA_SCORE_SOFTCAP) {
             // C log2(e) tanh(a s) = s Q(s^2), Q_k = C log2(e) a c_k a^(2k),
-            // valid while |a s| <= kTanhRange, i.e. s^2 <= s2_lim.
+            // valid while |a s| <= kTanhRange, i.e. |s| <= s_lim.
             cap_in = p.scale / p.score.softcap;
             cap_out = p.score.softcap * kLog2e;
             const float a2 = cap_in * cap_in;
@@ -381,228 +611,251 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             tq2 = base * a2 * a2 * kTanhC2;
             tq3 = base * a2 * a2 * a2 * kTanhC3;
             tq4 = base * a2 * a2 * a2 * a2 * kTanhC4;
-            s2_lim = (kTanhRange * kTanhRange) / a2;
+            s_lim = kTanhRange / cap_in;
         }
-        int* seg_tile = reinterpret_cast<int*>(smem + L::kSegTile);
-        uint32_t k = 0, t = 0, nu = 0, doc_tiles = 0;
+        int* seg_tile = reinterpret_cast<int*>(smem + L::kSegTile) + t * 256;
+        uint32_t k = 0, n = 0, uq = 0, doc_tiles = 0;
         bool ok = true;
         while (ok) {
             const uint32_t slot = k & 1;
             if (!mbar_wait_warp(bar(B_UNIT_FULL + slot), (k >> 1) & 1, wc, S_UNIT_FULL)) break;
-            const int u = unit_q[slot];
+            const int u = unit_q[2 * slot];
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_UNIT_EMPTY + slot));
             ++k;
             if (u < 0) break;
-            const Unit un = decode_unit(p, u);
-            const int i = un.qb * kBlock + r;
+            const Pair pu = decode_pair(p, u);
+            const int qb = 2 * pu.pr + t;
+            if (qb >= p.bm.nq) continue;            // an odd count of query blocks: no second tile
+            RowSeq rs;
+            rs.init(p, pu.b, pu.hq, qb);
+            const bool active = !rs.empty();
+            const int i = qb * kBlock + r;
             const int32_t* seg_row =
-                doc ? p.mask.seg + (size_t)(p.mask.seg_batch == 1 ? 0 : un.b) * p.mask.seg_len : nullptr;
+                doc ? p.mask.seg + (size_t)(p.mask.seg_batch == 1 ? 0 : pu.b) * p.mask.seg_len : nullptr;
             const int my_seg = (doc && i < p.q_len) ? seg_row[i] : 0;
             float slope_l2 = 0.f;
             const float* rb = nullptr;
-            if (SCORE == FA_SCORE_ALIBI) slope_l2 = p.score.slopes[un.hq] * kLog2e;
-            if (SCORE == FA_SCORE_REL_BIAS) rb = p.score.rel_bias + (size_t)un.hq * (2 * p.score.rel_max + 1);
-            int kb_next = un.n > 0 ? tile_kb(un, 0) : 0;
-            // this thread's segment id of the next partial tile, loaded a tile ahead
-            int seg_next = (doc && un.n_part > 0 && kb_next * kBlock + r < p.kv_len)
-                               ? __ldg(seg_row + kb_next * kBlock + r) : INT_MAX;
+            if (SCORE == FA_SCORE_ALIBI) slope_l2 = p.score.slopes[pu.hq] * kLog2e;
+            if (SCORE == FA_SCORE_REL_BIAS) rb = p.score.rel_bias + (size_t)pu.hq * (2 * p.score.rel_max + 1);
+            // this thread's segment id in the next partial tile, loaded a tile ahead
+            int seg_next = (doc && rs.hp != INT_MAX && rs.hp * kBlock + r < p.kv_len)
+                               ? __ldg(seg_row + rs.hp * kBlock + r) : INT_MAX;
 
             // m: the running row max (exact: every increase rescales O and
             // l, so the row's largest probability is exactly 1 and its bf16
             // rounding is exact); l: sum of the fp32 probabilities.
             float m_use = -CUDART_INF_F, l = 0.f;
-            for (int j = 0; j < un.n; ++j, ++t) {
-                const bool partial = j < un.n_part;
-                const int kb = kb_next;
-                if (j + 1 < un.n) kb_next = tile_kb(un, j + 1);
+            for (int j = 0; !rs.empty(); ++j, ++n) {
+                const int kb = rs.head();
+                const bool partial = rs.pop();
                 const int c0 = kb * kBlock;
                 int seg_lo = 0, seg_hi = -1;
                 if (partial && doc) {
                     // the tile's segment ids into shared memory (one per
                     // thread), then each row's visible columns by binary
-                    // search.  B_SEG counts the 128 writers; the buffer
+                    // search.  B_SEG + t counts the 128 writers; the buffer
                     // alternates, and a thread reaching document tile d+2 has
                     // seen every thread arrive at d+1, i.e. finish with d.
                     const uint32_t ph = doc_tiles & 1;
                     ++doc_tiles;
                     int* buf = seg_tile + ph * 128;
                     buf[r] = seg_next;
-                    mbar_arrive(bar(B_SEG));
-                    if (j + 1 < un.n_part)
-                        seg_next = kb_next * kBlock + r < p.kv_len ? __ldg(seg_row + kb_next * kBlock + r)
-                                                                    : INT_MAX;
-                    if (!mbar_wait_warp(bar(B_SEG), ph, wc, S_SEG)) { ok = false; break; }
+                    mbar_arrive(bar(B_SEG + t));
+                    seg_next = (rs.hp != INT_MAX && rs.hp * kBlock + r < p.kv_len)
+                                   ? __ldg(seg_row + rs.hp * kBlock + r) : INT_MAX;
+                    if (!mbar_wait_warp(bar(B_SEG + t), ph, wc, S_SEG)) { ok = false; break; }
                     seg_lo = count_below<true>(buf, my_seg);
                     seg_hi = count_below<false>(buf, my_seg) - 1;
                 }
-                if (!mbar_wait_warp(bar(B_S_FULL), t & 1, wc, S_S_FULL)) { ok = false; break; }
-                tc_fence_after();
-                float x[128];
-                {
-                    uint32_t raw[128];
-                    tmem_ld128(tS + lane_off, raw);
+                // The tile's two 64-column halves, each in its own S buffer:
+                // while this warpgroup works on one, the tensor pipe fills
+                // the other.
+#pragma unroll 1
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t tSh = tS + 64u * h;   // S_t,h; P_t,h in its first 32 columns
+                    const int ch = c0 + 64 * h;          // kv index of the half's column 0
+                    if (!mbar_wait_warp(bar(B_S_FULL + 2 * t + h), n & 1, wc, S_S_FULL)) { ok = false; break; }
+                    tc_fence_after();
+                    float x[64];
+                    {
+                        uint32_t raw[64];
+                        tmem_ld64(tSh + lane_off, raw);
 #pragma unroll
-                    for (int e = 0; e < 128; ++e) x[e] = __uint_as_float(raw[e]);
-                }
-
-                // score_mod on every visited element.  Without a score_mod x stays
-                // the raw q.k and the scale (times log2 e) is folded into the
-                // exponent's FMA; otherwise x is the modified score in base-2 units.
-                float sc = 1.f;
-                if (SCORE == FA_SCORE_NONE) {
-                    sc = sl2;
-                } else if (SCORE == FA_SCORE_SOFTCAP) {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        float wmax = 0.f;
-#pragma unroll
-                        for (int e = 0; e < 32; e += 2) {
-                            const int k = 32 * c + e;
-                            float w0, w1, q0, q1;
-                            fmul2(w0, w1, x[k], x[k + 1], x[k], x[k + 1]);
-                            wmax = fmax3(wmax, w0, w1);
-                            ffma2(q0, q1, w0, w1, tq4, tq4, tq3, tq3);
-                            ffma2(q0, q1, q0, q1, w0, w1, tq2, tq2);
-                            ffma2(q0, q1, q0, q1, w0, w1, tq1, tq1);
-                            ffma2(q0, q1, q0, q1, w0, w1, tq0, tq0);
-                            fmul2(x[k], x[k + 1], x[k], x[k + 1], q0, q1);
-                        }
-                        if (__any_sync(0xffffffffu, wmax > s2_lim)) {
-                            // some |u| beyond the polynomial's range: redo this
-                            // chunk from the raw scores still held in TMEM
-                            uint32_t raw[32];
-                            tmem_ld32(tS + lane_off + 32u * c, raw);
-#pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                x[32 * c + e] = softcap_exact(__uint_as_float(raw[e]) * cap_in, cap_out);
-                        }
+                        for (int e = 0; e < 64; ++e) x[e] = __uint_as_float(raw[e]);
                     }
-                } else if (SCORE == FA_SCORE_ALIBI) {
-                    // bias -slope |i - j|; when every (row, column) pair of the
-                    // warp's rows lies on one side of the diagonal it is affine in
-                    // the column and takes one packed FMA per pair.
-                    const float di = static_cast<float>(i - c0);
-                    const int wrow0 = un.qb * kBlock + warp * 32 - c0;     // i - c0 of lane 0
-                    if (wrow0 - (kBlock - 1) >= 0 || wrow0 + 31 <= 0) {
-                        const float sgn = wrow0 >= 0 ? 1.f : -1.f;       // sign of i - j
-                        const float k0 = -sgn * slope_l2 * di, ks = sgn * slope_l2;
+
+                    // score_mod on every visited element.  Without a score_mod
+                    // x stays the raw q.k and the scale (times log2 e) is folded
+                    // into the exponent's FMA; otherwise x is the modified score
+                    // in base-2 units.
+                    float sc = 1.f;
+                    if (SCORE == FA_SCORE_NONE) {
+                        sc = sl2;
+                    } else if (SCORE == FA_SCORE_SOFTCAP) {
+                        // The polynomial holds while |s| <= s_lim.  One pass of
+                        // |x| maxima decides, for the warp's 32 rows at once,
+                        // between it and the exact form (rare for soft-cap
+                        // workloads: |s| reaches s_lim only for large logits).
+                        float am[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                        for (int e = 0; e < 128; e += 2) {
-                            float b0, b1;
-                            ffma2(b0, b1, ks, ks, static_cast<float>(e), static_cast<float>(e + 1), k0, k0);
-                            ffma2(x[e], x[e + 1], x[e], x[e + 1], sl2, sl2, b0, b1);
+                        for (int e = 0; e < 64; e += 8) {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) am[q] = fmax3(am[q], fabsf(x[e + q]), fabsf(x[e + 4 + q]));
+                        }
+                        const float amax = fmax3(fmaxf(am[0], am[1]), am[2], am[3]);
+                        if (!__any_sync(0xffffffffu, amax > s_lim)) {
+#pragma unroll
+                            for (int e = 0; e < 64; e += 2) {
+                                float w0, w1, q0, q1;
+                                fmul2(w0, w1, x[e], x[e + 1], x[e], x[e + 1]);
+                                ffma2(q0, q1, w0, w1, tq4, tq4, tq3, tq3);
+                                ffma2(q0, q1, q0, q1, w0, w1, tq2, tq2);
+                                ffma2(q0, q1, q0, q1, w0, w1, tq1, tq1);
+                                ffma2(q0, q1, q0, q1, w0, w1, tq0, tq0);
+                                fmul2(x[e], x[e + 1], x[e], x[e + 1], q0, q1);
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 64; ++e) x[e] = softcap_exact(x[e] * cap_in, cap_out);
+                        }
+                    } else if (SCORE == FA_SCORE_ALIBI) {
+                        // bias -slope |i - j|; when every (row, column) pair of
+                        // the warp's rows and the half's columns lies on one side
+                        // of the diagonal it is affine in the column and takes one
+                        // packed FMA per pair.
+                        const float di = static_cast<float>(i - ch);
+                        const int wrow0 = qb * kBlock + wq * 32 - ch;     // i - ch of lane 0
+                        if (wrow0 - 63 >= 0 || wrow0 + 31 <= 0) {
+                            const float sgn = wrow0 >= 0 ? 1.f : -1.f;   // sign of i - j
+                            const float k0 = -sgn * slope_l2 * di, ks = sgn * slope_l2;
+#pragma unroll
+                            for (int e = 0; e < 64; e += 2) {
+                                float b0, b1;
+                                ffma2(b0, b1, ks, ks, static_cast<float>(e), static_cast<float>(e + 1), k0, k0);
+                                ffma2(x[e], x[e + 1], x[e], x[e + 1], sl2, sl2, b0, b1);
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 64; ++e)
+                                x[e] = fmaf(-slope_l2, fabsf(di - static_cast<float>(e)), x[e] * sl2);
                         }
                     } else {
 #pragma unroll
-                        for (int e = 0; e < 128; ++e)
-                            x[e] = fmaf(-slope_l2, fabsf(di - static_cast<float>(e)), x[e] * sl2);
-                    }
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 128; ++e) {
-                        const int rr = min(max(i - c0 - e, -p.score.rel_max), p.score.rel_max);
-                        x[e] = fmaf(__ldg(rb + rr + p.score.rel_max), kLog2e, x[e] * sl2);
-                    }
-                }
-
-                // mask_mod only on partial tiles.  Every built-in predicate leaves,
-                // per row, one interval of visible columns [lo, hi]: causal
-                // [0, i], window [i - W, i], prefix-LM [0, max(i, P - 1)], and for
-                // a document mask (ids non-decreasing) the columns whose id equals
-                // the row's (found above by binary search in the tile's ids).
-                if (partial) {
-                    int lo = -c0, hi = p.kv_len - 1 - c0;
-                    if (doc) {
-                        lo = seg_lo;
-                        hi = min(hi, seg_hi);
-                    } else if (p.mask.kind == FA_MASK_CAUSAL) {
-                        hi = min(hi, i - c0);
-                    } else if (p.mask.kind == FA_MASK_SLIDING_WINDOW) {
-                        hi = min(hi, i - c0);
-                        lo = i - p.mask.window - c0;
-                    } else if (p.mask.kind == FA_MASK_PREFIX_LM) {
-                        hi = min(hi, max(i, p.mask.prefix_len - 1) - c0);
-                    }
-#pragma unroll
-                    for (int e = 0; e < 128; ++e) x[e] = (e >= lo && e <= hi) ? x[e] : -CUDART_INF_F;
-                }
-
-                // row max: four independent chains of 3-input max
-                float m4[4] = {x[0], x[1], x[2], x[3]};
-#pragma unroll
-                for (int e = 4; e < 128; e += 8) {
-#pragma unroll
-                    for (int t = 0; t < 4; ++t) m4[t] = fmax3(m4[t], x[e + t], x[e + 4 + t]);
-                }
-                const float mx = fmax3(fmaxf(m4[0], m4[1]), m4[2], m4[3]) * sc;
-                const float m_new = fmaxf(m_use, mx);
-                // O and l follow every increase of the max.  O holds the PV
-                // products of tiles 0..j-1 (all complete: the S commit of
-                // tile j tracks every earlier MMA); its rescale is interleaved
-                // with the exponentials below so that the TMEM round trips
-                // overlap arithmetic.
-                const bool need = j > 0 && m_new > m_use;
-                const float alpha = need ? ex2_approx(m_use - m_new) : 1.f;
-                if (need) l *= alpha;
-                m_use = m_new;
-                const bool rescale = __any_sync(0xffffffffu, need);
-                const float nm = m_use == -CUDART_INF_F ? 0.f : -m_use;
-
-                // P = 2^(x sc - m) -> bf16 pairs into TMEM over S, 32 columns
-                // of S (16 of P) at a time.
-                float rs[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t o[32];
-                    const bool oc = rescale && c < D / 32;
-                    if (oc) tmem_ld32_async(tO + lane_off + 32u * c, o);
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int col = 32 * c + 2 * e;
-                        float p0, p1;
-                        exp_pair<false>(p0, p1, x[col], x[col + 1], sc, nm);
-                        const int a2 = (e & 1) * 2;
-                        fadd2(rs[a2], rs[a2 + 1], rs[a2], rs[a2 + 1], p0, p1);
-                        pk[e] = pack_bf16x2(p0, p1);
-                    }
-                    if (oc) {
-                        tmem_wait_ld(o);
-#pragma unroll
-                        for (int e = 0; e < 32; e += 2) {
-                            float a0, a1;
-                            fmul2(a0, a1, __uint_as_float(o[e]), __uint_as_float(o[e + 1]), alpha, alpha);
-                            o[e] = __float_as_uint(a0);
-                            o[e + 1] = __float_as_uint(a1);
+                        for (int e = 0; e < 64; ++e) {
+                            const int rr = min(max(i - ch - e, -p.score.rel_max), p.score.rel_max);
+                            x[e] = fmaf(__ldg(rb + rr + p.score.rel_max), kLog2e, x[e] * sl2);
                         }
-                        tmem_st32(tO + lane_off + 32u * c, o);
                     }
-                    tmem_st16(tP + lane_off + 16u * c, pk);
-                }
-                l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
 
-                tc_fence_before();
-                mbar_arrive(bar(B_P_FULL));
+                    // mask_mod only on partial tiles.  Every built-in predicate
+                    // leaves, per row, one interval of visible columns [lo, hi]:
+                    // causal [0, i], window [i - W, i], prefix-LM
+                    // [0, max(i, P - 1)], and for a document mask (ids
+                    // non-decreasing) the columns whose id equals the row's
+                    // (found above by binary search in the tile's ids).
+                    if (partial) {
+                        int lo = -ch, hi = p.kv_len - 1 - ch;
+                        if (doc) {
+                            lo = seg_lo - 64 * h;
+                            hi = min(hi, seg_hi - 64 * h);
+                        } else if (p.mask.kind == FA_MASK_CAUSAL) {
+                            hi = min(hi, i - ch);
+                        } else if (p.mask.kind == FA_MASK_SLIDING_WINDOW) {
+                            hi = min(hi, i - ch);
+                            lo = i - p.mask.window - ch;
+                        } else if (p.mask.kind == FA_MASK_PREFIX_LM) {
+                            hi = min(hi, max(i, p.mask.prefix_len - 1) - ch);
+                        }
+#pragma unroll
+                        for (int e = 0; e < 64; ++e) x[e] = (e >= lo && e <= hi) ? x[e] : -CUDART_INF_F;
+                    }
+
+                    // row max: four independent chains of 3-input max
+                    float m4[4] = {x[0], x[1], x[2], x[3]};
+#pragma unroll
+                    for (int e = 4; e < 64; e += 8) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) m4[q] = fmax3(m4[q], x[e + q], x[e + 4 + q]);
+                    }
+                    const float mx = fmax3(fmaxf(m4[0], m4[1]), m4[2], m4[3]) * sc;
+                    const float m_new = fmaxf(m_use, mx);
+                    // O and l follow every increase of the max
+                    const bool need = (j > 0 || h > 0) && m_new > m_use;
+                    const float alpha = need ? ex2_approx(m_use - m_new) : 1.f;
+                    if (need) l *= alpha;
+                    m_use = m_new;
+                    const float nm = m_use == -CUDART_INF_F ? 0.f : -m_use;
+
+                    // P = 2^(x sc - m) -> bf16 pairs into TMEM over S_t,h
+                    float rs[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int col = 32 * c + 2 * e;
+                            float p0, p1;
+                            exp_pair<false>(p0, p1, x[col], x[col + 1], sc, nm);
+                            const int a2 = (e & 1) * 2;
+                            fadd2(rs[a2], rs[a2 + 1], rs[a2], rs[a2 + 1], p0, p1);
+                            pk[e] = pack_bf16x2(p0, p1);
+                        }
+                        tmem_st16_nowait(tSh + lane_off + 16u * c, pk);
+                    }
+                    l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+
+                    // O holds the products of this tile's earlier halves; the
+                    // previous one's may still be running (its P was released
+                    // just before this S was read), so wait for it (O_UPD
+                    // counts every product of the tile; 2 n + h halves of the
+                    // tile came before this one) and scale.
+                    if (__any_sync(0xffffffffu, need)) {
+                        const uint32_t prev = 2 * n + h - 1;
+                        if (!mbar_wait_warp(bar(B_O_UPD + t), prev & 1, wc, S_O_UPD)) { ok = false; break; }
+                        tc_fence_after();
+                        uint32_t o[D / 32][32];
+#pragma unroll
+                        for (int c = 0; c < D / 32; ++c) tmem_ld32_async(tO + lane_off + 32u * c, o[c]);
+#pragma unroll
+                        for (int c = 0; c < D / 32; ++c) tmem_wait_ld(o[c]);
+#pragma unroll
+                        for (int c = 0; c < D / 32; ++c) {
+#pragma unroll
+                            for (int e = 0; e < 32; e += 2) {
+                                float a0, a1;
+                                fmul2(a0, a1, __uint_as_float(o[c][e]), __uint_as_float(o[c][e + 1]), alpha, alpha);
+                                o[c][e] = __float_as_uint(a0);
+                                o[c][e + 1] = __float_as_uint(a1);
+                            }
+                            tmem_st32_nowait(tO + lane_off + 32u * c, o[c]);
+                        }
+                    }
+                    // P (and a scaled O) must be in TMEM before the MMA may read it
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(bar(B_P_FULL + 2 * t + h));
+                }
+                if (!ok) break;
             }
             if (!ok) break;
 
             // epilogue: O / l and lse = (m + log2 l) ln 2; a row that saw no
             // key gets O = 0 and lse = -inf.
-            if (un.n > 0) {
-                if (!mbar_wait_warp(bar(B_O_FULL), nu & 1, wc, S_O_FULL)) break;
+            if (active) {
+                if (!mbar_wait_warp(bar(B_O_DONE + t), uq & 1, wc, S_O_DONE)) break;
                 tc_fence_after();
-                ++nu;
+                ++uq;
             }
             const bool empty = !(l > 0.f);
             const float inv = empty ? 0.f : 1.f / l;
             const bool row_ok = i < p.q_len;
             const bool out32 = (p.flags & FA_OUT_FP32) != 0;
-            const size_t row_elem = (((size_t)un.b * p.Hq + un.hq) * p.q_len + i) * D;
+            const size_t row_elem = (((size_t)pu.b * p.Hq + pu.hq) * p.q_len + i) * D;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
-                if (un.n > 0) {
+                if (active) {
                     tmem_ld32(tO + lane_off + 32u * c, o);
                 } else {
 #pragma unroll
@@ -627,7 +880,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 }
             }
             if (row_ok)
-                p.lse[((size_t)un.b * p.Hq + un.hq) * p.q_len + i] =
+                p.lse[((size_t)pu.b * p.Hq + pu.hq) * p.q_len + i] =
                     empty ? -CUDART_INF_F : (m_use + log2f(l)) * kLn2;
         }
         tc_fence_before();
@@ -655,9 +908,12 @@ cudaError_t launch_one(const FwdParams& p, const CUtensorMap& tq, const CUtensor
         if (e != cudaSuccess) return e;
     }
     const int sms = (dev >= 0 && dev < 64) ? sm_count[dev] : 148;
-    // persistent: two CTAs per SM (or fewer if there are fewer units)
-    const long long grid = std::min<long long>(p.num_units, 2LL * sms);
-    kern<<<(unsigned)grid, kThreads, smem, s>>>(tq, tk, tv, p);
+    // persistent: one CTA per SM (or fewer if there are fewer units); a
+    // unit is a pair of query blocks
+    FwdParams q = p;
+    q.num_units = p.B * p.Hq * ((p.bm.nq + 1) / 2);
+    const long long grid = std::min<long long>(q.num_units, sms);
+    kern<<<(unsigned)grid, kThreads, smem, s>>>(tq, tk, tv, q);
     return cudaGetLastError();
 }
 
