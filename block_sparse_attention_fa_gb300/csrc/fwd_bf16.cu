@@ -73,10 +73,10 @@ enum Bar {
     B_K_FULL = 4, B_K_EMPTY = B_K_FULL + kMaxStages,
     B_V_FULL = B_K_EMPTY + kMaxStages, B_V_EMPTY = B_V_FULL + kMaxStages,
     B_S_FULL = B_V_EMPTY + kMaxStages,          // four (2 t + h): MMA commit of S_t,h
-    B_P_FULL = B_S_FULL + 4,                    // four (2 t + h): 128 softmax threads of tile t
+    B_P_FULL = B_S_FULL + 4,                    // four (2 t + h): the 4 softmax warps of tile t
     B_O_DONE = B_P_FULL + 4,                    // two: MMA commit after a unit's last P_t V
     B_O_UPD = B_O_DONE + 2,                     // two: MMA commit after every P_t V
-    B_SEG = B_O_UPD + 2,                        // two: 128 softmax threads, per document tile
+    B_SEG = B_O_UPD + 2,                        // two: the 4 softmax warps of tile t, per document tile
     B_UNIT_FULL = B_SEG + 2,                    // two slots
     B_UNIT_EMPTY = B_UNIT_FULL + 2,             // two slots
     B_DRAIN = B_UNIT_EMPTY + 2,                 // two: one per MMA warp
@@ -86,6 +86,12 @@ enum Site : uint32_t { S_Q = 1, S_Q_EMPTY, S_K_FULL, S_K_EMPTY, S_V_FULL, S_V_EM
                        S_P_FULL, S_O_DONE, S_DRAIN, S_LOAD_DRAIN, S_SEG, S_UNIT_FULL, S_UNIT_EMPTY,
                        S_O_UPD };
 constexpr uint32_t kUnitConsumers = 10;   // one lane of each MMA warp and of each softmax warp
+// A unit-queue slot: the unit (-1 = none left), whether its pair visits any
+// kv tile, and for each query tile its BlockMask row's list lengths and first
+// entries (read by the loader, so that no other role waits for them).
+constexpr int kUnitWords = 14;
+// UW_ROW + 6 t + {n_part, n_full, part[n_part - 1], part[n_part - 2], full[n_full - 1], full[n_full - 2]}
+enum UnitWord { UW_UNIT = 0, UW_HAS_STEPS = 1, UW_ROW = 2 };
 
 // Which columns of a full tile take their exponential on the FMA pipe (the
 // polynomial below) instead of the MUFU ex2 unit: columns with
@@ -161,10 +167,14 @@ struct Layout {
     static constexpr uint32_t kBars = kV + kStages * kTile;
     static constexpr uint32_t kTmemSlot = kBars + 8 * B_COUNT;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
-    static constexpr uint32_t kUnitQ = kAbort + 4;        // 2 slots x (unit, has steps)
-    static constexpr uint32_t kStepFlags = kUnitQ + 16;   // kStages x uint32: flags of each stage's step
+    static constexpr uint32_t kUnitQ = kAbort + 4;        // 2 slots x kUnitWords int32
+    static constexpr uint32_t kStepFlags = kUnitQ + 2 * 4 * kUnitWords;  // kStages x uint32: flags of each stage's step
     static constexpr uint32_t kSegTile = (kStepFlags + 4 * kMaxStages + 15) & ~15u;  // [2 tiles][2][128] int32
-    static constexpr uint32_t kUsed = kSegTile + 2 * 2 * 128 * 4;
+    // per softmax warp, 32 rows x 64 bytes of O (+16 bytes of padding per row,
+    // so that row-wise writes and the 4-lanes-per-row reads hit distinct banks)
+    static constexpr uint32_t kOStageRow = 80;
+    static constexpr uint32_t kOStage = kSegTile + 2 * 2 * 128 * 4;
+    static constexpr uint32_t kUsed = kOStage + 8 * 32 * kOStageRow;
     static constexpr uint32_t kDynamic = kUsed + 1024;    // + 1 KB to align the base to 1024
     static_assert(kDynamic <= 227u * 1024u, "shared memory budget");
     static_assert(kStages <= kMaxStages, "too many stages");
@@ -207,43 +217,68 @@ __device__ __forceinline__ Pair decode_pair(const FwdParams& p, int u) {
     return x;
 }
 
-// The kv tiles of one BlockMask row in ascending order: the row's partial
-// and full lists (each ascending, disjoint) merged as they are walked.  The
-// next entry of a list is loaded when its head is taken, a whole step before
-// it is compared.  A query block past the last one has no tiles.
+// The kv tiles of one BlockMask row in DESCENDING order: the row's partial
+// and full lists (each ascending, disjoint) merged as they are walked from
+// their ends.  For causal, window and ALiBi rows the largest scores sit near
+// the diagonal, so the running max settles on the first tiles and O is seldom
+// rescaled afterwards.  Each list keeps its next two entries in registers,
+// and taking an entry requests the one after them, which is first compared a
+// step later: no step waits for a load.  A query block past the last one has
+// no tiles.
 struct RowSeq {
     const int32_t* part;
     const int32_t* full;
-    int n_part, n_full, ip, jf;
-    int hp, hf;    // heads: next partial / full kv block, INT_MAX when done
+    int ip, jf;              // indices of the next partial / full entry (-1: done)
+    int p0, p1, f0, f1;      // part[ip], part[ip - 1], full[jf], full[jf - 1] as read
 
+    __device__ __forceinline__ void set_row(const FwdParams& p, int b, int hq, int qb) {
+        const int mb = p.bm.B == 1 ? 0 : b, mh = p.bm.H == 1 ? 0 : hq;
+        const size_t mrow = ((size_t)mb * p.bm.H + mh) * p.bm.nq + min(qb, p.bm.nq - 1);
+        part = p.bm.kv_indices + mrow * p.bm.nkv;
+        full = p.bm.full_kv_indices + mrow * p.bm.nkv;
+    }
+    // From the values the loader has already read:
+    // w = {n_part, n_full, part[n_part - 1], part[n_part - 2], full[n_full - 1], full[n_full - 2]}.
+    __device__ __forceinline__ void init_from(const FwdParams& p, int b, int hq, int qb, const volatile int* w) {
+        set_row(p, b, hq, qb);
+        ip = w[0] - 1;
+        jf = w[1] - 1;
+        p0 = w[2];
+        p1 = w[3];
+        f0 = w[4];
+        f1 = w[5];
+    }
     __device__ __forceinline__ void init(const FwdParams& p, int b, int hq, int qb) {
-        ip = jf = 0;
-        n_part = n_full = 0;
-        part = full = nullptr;
-        hp = hf = INT_MAX;
+        set_row(p, b, hq, qb);
+        ip = jf = -1;
+        p0 = p1 = f0 = f1 = -1;
         if (qb >= p.bm.nq) return;
         const int mb = p.bm.B == 1 ? 0 : b, mh = p.bm.H == 1 ? 0 : hq;
         const size_t mrow = ((size_t)mb * p.bm.H + mh) * p.bm.nq + qb;
-        n_part = __ldg(p.bm.kv_num_blocks + mrow);
-        n_full = __ldg(p.bm.full_kv_num_blocks + mrow);
-        part = p.bm.kv_indices + mrow * p.bm.nkv;
-        full = p.bm.full_kv_indices + mrow * p.bm.nkv;
-        if (n_part > 0) hp = __ldg(part);
-        if (n_full > 0) hf = __ldg(full);
+        ip = __ldg(p.bm.kv_num_blocks + mrow) - 1;
+        jf = __ldg(p.bm.full_kv_num_blocks + mrow) - 1;
+        p0 = __ldg(part + max(ip, 0));
+        p1 = __ldg(part + max(ip - 1, 0));
+        f0 = __ldg(full + max(jf, 0));
+        f1 = __ldg(full + max(jf - 1, 0));
     }
-    // (by the counts, so that it never waits for the head just requested)
-    __device__ __forceinline__ bool empty() const { return ip >= n_part && jf >= n_full; }
-    __device__ __forceinline__ int head() const { return min(hp, hf); }
+    __device__ __forceinline__ int n_part() const { return ip + 1; }
+    __device__ __forceinline__ int n_full() const { return jf + 1; }
+    __device__ __forceinline__ bool empty() const { return ip < 0 && jf < 0; }
+    __device__ __forceinline__ int next_part() const { return ip >= 0 ? p0 : -1; }
+    __device__ __forceinline__ int next_full() const { return jf >= 0 ? f0 : -1; }
+    __device__ __forceinline__ int head() const { return max(next_part(), next_full()); }
     // Takes the head; returns whether it was a partial tile.
     __device__ __forceinline__ bool pop() {
-        if (hp < hf) {
-            ++ip;
-            hp = ip < n_part ? __ldg(part + ip) : INT_MAX;
+        if (next_part() > next_full()) {
+            --ip;
+            p0 = p1;
+            p1 = __ldg(part + max(ip - 1, 0));
             return true;
         }
-        ++jf;
-        hf = jf < n_full ? __ldg(full + jf) : INT_MAX;
+        --jf;
+        f0 = f1;
+        f1 = __ldg(full + max(jf - 1, 0));
         return false;
     }
 };
@@ -253,7 +288,7 @@ constexpr uint32_t kInTile0 = 1u;         // << t: query tile t visits the step'
 constexpr uint32_t kLastOfTile0 = 4u;     // << t: and it is tile t's last of the unit
 constexpr uint32_t kLastOfUnit = 16u;     // no step follows in this unit
 
-// The pair's sequence: the union of the two rows' tiles, ascending.  Each
+// The pair's sequence: the union of the two rows' tiles, descending.  Each
 // step names one kv block and, in its flags, which of the two query tiles
 // visit it.
 struct PairSeq {
@@ -265,7 +300,7 @@ struct PairSeq {
     __device__ __forceinline__ bool empty() const { return row[0].empty() && row[1].empty(); }
     __device__ __forceinline__ bool next(int& kb, uint32_t& flags) {
         if (empty()) return false;
-        kb = min(row[0].head(), row[1].head());
+        kb = max(row[0].head(), row[1].head());
         flags = 0;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
@@ -300,7 +335,8 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     if (threadIdx.x == 0) {
         for (int k = 0; k < B_COUNT; ++k) {
             uint32_t cnt = 1;
-            if ((k >= B_P_FULL && k < B_P_FULL + 4) || k == B_SEG || k == B_SEG + 1) cnt = 128;
+            // one arrival per softmax warp of the tile
+            if ((k >= B_P_FULL && k < B_P_FULL + 4) || k == B_SEG || k == B_SEG + 1) cnt = 4;
             if (k == B_UNIT_EMPTY || k == B_UNIT_EMPTY + 1) cnt = kUnitConsumers;
             // a stage is free once both MMA warps have released it
             if (k >= B_K_EMPTY && k < B_K_EMPTY + kMaxStages) cnt = 2;
@@ -351,8 +387,20 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     pu = decode_pair(p, u);
                     seq.init(p, pu);
                 }
-                unit_q[2 * slot] = u;
-                unit_q[2 * slot + 1] = u >= 0 && !seq.empty();
+                volatile int* qs = unit_q + kUnitWords * slot;
+                qs[UW_UNIT] = u;
+                qs[UW_HAS_STEPS] = u >= 0 && !seq.empty();
+                if (u >= 0) {
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        qs[UW_ROW + 6 * t + 0] = seq.row[t].n_part();
+                        qs[UW_ROW + 6 * t + 1] = seq.row[t].n_full();
+                        qs[UW_ROW + 6 * t + 2] = seq.row[t].p0;
+                        qs[UW_ROW + 6 * t + 3] = seq.row[t].p1;
+                        qs[UW_ROW + 6 * t + 4] = seq.row[t].f0;
+                        qs[UW_ROW + 6 * t + 5] = seq.row[t].f1;
+                    }
+                }
                 mbar_arrive(bar(B_UNIT_FULL + slot));
                 ++k;
                 if (u < 0) break;
@@ -480,8 +528,8 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             while (ok) {
                 const uint32_t slot = k & 1;
                 if (!mbar_wait_warp(bar(B_UNIT_FULL + slot), (k >> 1) & 1, wc, S_UNIT_FULL)) break;
-                const int u = unit_q[2 * slot];
-                const bool has_steps = unit_q[2 * slot + 1] != 0;
+                const int u = unit_q[kUnitWords * slot + UW_UNIT];
+                const bool has_steps = unit_q[kUnitWords * slot + UW_HAS_STEPS] != 0;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_UNIT_EMPTY + slot));
                 ++k;
@@ -616,31 +664,58 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         int* seg_tile = reinterpret_cast<int*>(smem + L::kSegTile) + t * 256;
         uint32_t k = 0, n = 0, uq = 0, doc_tiles = 0;
         bool ok = true;
-        while (ok) {
+        // A unit as this warpgroup sees it.  The next unit is taken from the
+        // queue before the current one's epilogue, so that its per-thread
+        // loads (segment ids, slope) are in flight while the epilogue runs;
+        // the BlockMask row itself comes from the queue slot.
+        struct Cur {
+            int u, qb, i, my_seg, seg_next;
+            float slope_l2;
+            Pair pu;
+            RowSeq rs;
+        };
+        auto take = [&](Cur& c) -> bool {
             const uint32_t slot = k & 1;
-            if (!mbar_wait_warp(bar(B_UNIT_FULL + slot), (k >> 1) & 1, wc, S_UNIT_FULL)) break;
-            const int u = unit_q[2 * slot];
+            if (!mbar_wait_warp(bar(B_UNIT_FULL + slot), (k >> 1) & 1, wc, S_UNIT_FULL)) return false;
+            const volatile int* qs = unit_q + kUnitWords * slot;
+            c.u = qs[UW_UNIT];
+            c.qb = 0;
+            if (c.u >= 0) {
+                c.pu = decode_pair(p, c.u);
+                c.qb = 2 * c.pu.pr + t;
+                c.rs.init_from(p, c.pu.b, c.pu.hq, c.qb, qs + UW_ROW + 6 * t);
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_UNIT_EMPTY + slot));
             ++k;
-            if (u < 0) break;
-            const Pair pu = decode_pair(p, u);
-            const int qb = 2 * pu.pr + t;
-            if (qb >= p.bm.nq) continue;            // an odd count of query blocks: no second tile
-            RowSeq rs;
-            rs.init(p, pu.b, pu.hq, qb);
+            if (c.u < 0 || c.qb >= p.bm.nq) return true;
+            c.i = c.qb * kBlock + r;
+            const int32_t* seg_row =
+                doc ? p.mask.seg + (size_t)(p.mask.seg_batch == 1 ? 0 : c.pu.b) * p.mask.seg_len : nullptr;
+            c.my_seg = (doc && c.i < p.q_len) ? __ldg(seg_row + c.i) : 0;
+            // this thread's segment id in the first partial tile
+            const int kp = c.rs.next_part();
+            c.seg_next = (doc && kp >= 0 && kp * kBlock + r < p.kv_len) ? __ldg(seg_row + kp * kBlock + r) : INT_MAX;
+            c.slope_l2 = SCORE == FA_SCORE_ALIBI ? __ldg(p.score.slopes + c.pu.hq) * kLog2e : 0.f;
+            return true;
+        };
+        Cur cur;
+        if (!take(cur)) ok = false;
+        while (ok && cur.u >= 0) {
+            if (cur.qb >= p.bm.nq) {                // an odd count of query blocks: no second tile
+                if (!take(cur)) ok = false;
+                continue;
+            }
+            const Pair pu = cur.pu;
+            const int qb = cur.qb, i = cur.i, my_seg = cur.my_seg;
+            RowSeq rs = cur.rs;
+            int seg_next = cur.seg_next;
+            const float slope_l2 = cur.slope_l2;
             const bool active = !rs.empty();
-            const int i = qb * kBlock + r;
             const int32_t* seg_row =
                 doc ? p.mask.seg + (size_t)(p.mask.seg_batch == 1 ? 0 : pu.b) * p.mask.seg_len : nullptr;
-            const int my_seg = (doc && i < p.q_len) ? seg_row[i] : 0;
-            float slope_l2 = 0.f;
             const float* rb = nullptr;
-            if (SCORE == FA_SCORE_ALIBI) slope_l2 = p.score.slopes[pu.hq] * kLog2e;
             if (SCORE == FA_SCORE_REL_BIAS) rb = p.score.rel_bias + (size_t)pu.hq * (2 * p.score.rel_max + 1);
-            // this thread's segment id in the next partial tile, loaded a tile ahead
-            int seg_next = (doc && rs.hp != INT_MAX && rs.hp * kBlock + r < p.kv_len)
-                               ? __ldg(seg_row + rs.hp * kBlock + r) : INT_MAX;
 
             // m: the running row max (exact: every increase rescales O and
             // l, so the row's largest probability is exactly 1 and its bf16
@@ -654,16 +729,19 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 if (partial && doc) {
                     // the tile's segment ids into shared memory (one per
                     // thread), then each row's visible columns by binary
-                    // search.  B_SEG + t counts the 128 writers; the buffer
-                    // alternates, and a thread reaching document tile d+2 has
-                    // seen every thread arrive at d+1, i.e. finish with d.
+                    // search.  B_SEG + t counts the tile's 4 warps (each
+                    // arrives once its 32 ids are written); the buffer
+                    // alternates, and a warp reaching document tile d+2 has
+                    // seen every warp arrive at d+1, i.e. finish with d.
                     const uint32_t ph = doc_tiles & 1;
                     ++doc_tiles;
                     int* buf = seg_tile + ph * 128;
                     buf[r] = seg_next;
-                    mbar_arrive(bar(B_SEG + t));
-                    seg_next = (rs.hp != INT_MAX && rs.hp * kBlock + r < p.kv_len)
-                                   ? __ldg(seg_row + rs.hp * kBlock + r) : INT_MAX;
+                    __threadfence_block();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(B_SEG + t));
+                    const int kp = rs.next_part();
+                    seg_next = (kp >= 0 && kp * kBlock + r < p.kv_len) ? __ldg(seg_row + kp * kBlock + r) : INT_MAX;
                     if (!mbar_wait_warp(bar(B_SEG + t), ph, wc, S_SEG)) { ok = false; break; }
                     seg_lo = count_below<true>(buf, my_seg);
                     seg_hi = count_below<false>(buf, my_seg) - 1;
@@ -834,11 +912,16 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     // P (and a scaled O) must be in TMEM before the MMA may read it
                     tmem_wait_st();
                     tc_fence_before();
-                    mbar_arrive(bar(B_P_FULL + 2 * t + h));
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(B_P_FULL + 2 * t + h));
                 }
                 if (!ok) break;
             }
             if (!ok) break;
+
+            // the next unit, before this one's epilogue
+            Cur nxt;
+            if (!take(nxt)) break;
 
             // epilogue: O / l and lse = (m + log2 l) ln 2; a row that saw no
             // key gets O = 0 and lse = -inf.
@@ -851,37 +934,60 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const float inv = empty ? 0.f : 1.f / l;
             const bool row_ok = i < p.q_len;
             const bool out32 = (p.flags & FA_OUT_FP32) != 0;
-            const size_t row_elem = (((size_t)pu.b * p.Hq + pu.hq) * p.q_len + i) * D;
+            // O leaves in 64-byte column chunks (32 bf16 or 16 fp32 columns)
+            // through this warp's staging rows in shared memory, so that each
+            // global store instruction writes 8 rows x 64 contiguous bytes
+            // instead of 32 scattered 16-byte pieces.
+            uint8_t* stage = smem + L::kOStage + warp * 32 * L::kOStageRow;
+            const size_t head_row0 = ((size_t)pu.b * p.Hq + pu.hq) * p.q_len;
+            const int rows_left = p.q_len - (qb * kBlock + wq * 32);   // rows of this warp that exist
+            const int nchunk = out32 ? D / 16 : D / 32;
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t o[32];
-                if (active) {
-                    tmem_ld32(tO + lane_off + 32u * c, o);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = 0u;
-                }
-#pragma unroll
-                for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * inv);
-                if (!row_ok) continue;
+            for (int c = 0; c < nchunk; ++c) {
+                uint32_t w[16];
                 if (out32) {
-                    uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(p.o) + row_elem + 32 * c);
+                    uint32_t o[16];
+                    if (active) {
+                        tmem_ld16(tO + lane_off + 16u * c, o);
+                    } else {
 #pragma unroll
-                    for (int v = 0; v < 8; ++v) dst[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+                        for (int e = 0; e < 16; ++e) o[e] = 0u;
+                    }
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(__uint_as_float(o[e]) * inv);
                 } else {
-                    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + row_elem + 32 * c);
+                    uint32_t o[32];
+                    if (active) {
+                        tmem_ld32(tO + lane_off + 32u * c, o);
+                    } else {
 #pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        dst[v] = make_uint4(
-                            pack_bf16x2(__uint_as_float(o[8 * v + 0]), __uint_as_float(o[8 * v + 1])),
-                            pack_bf16x2(__uint_as_float(o[8 * v + 2]), __uint_as_float(o[8 * v + 3])),
-                            pack_bf16x2(__uint_as_float(o[8 * v + 4]), __uint_as_float(o[8 * v + 5])),
-                            pack_bf16x2(__uint_as_float(o[8 * v + 6]), __uint_as_float(o[8 * v + 7])));
+                        for (int e = 0; e < 32; ++e) o[e] = 0u;
+                    }
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+                }
+                __syncwarp();    // the previous chunk's reads of the staging rows are done
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    *reinterpret_cast<uint4*>(stage + lane * L::kOStageRow + 16 * q) =
+                        make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+                __syncwarp();
+#pragma unroll
+                for (int it = 0; it < 4; ++it) {
+                    const int row = it * 8 + (lane >> 2), piece = lane & 3;
+                    if (row < rows_left) {
+                        const uint4 v = *reinterpret_cast<const uint4*>(stage + row * L::kOStageRow + 16 * piece);
+                        const size_t grow = head_row0 + (size_t)(qb * kBlock + wq * 32 + row);
+                        uint8_t* dst = static_cast<uint8_t*>(p.o) + grow * D * (out32 ? 4 : 2) + 64 * c + 16 * piece;
+                        *reinterpret_cast<uint4*>(dst) = v;
+                    }
                 }
             }
             if (row_ok)
                 p.lse[((size_t)pu.b * p.Hq + pu.hq) * p.q_len + i] =
                     empty ? -CUDART_INF_F : (m_use + log2f(l)) * kLn2;
+            cur = nxt;
         }
         tc_fence_before();
         __syncthreads();
