@@ -129,19 +129,29 @@ __device__ __forceinline__ float softcap_exact(float u, float cap_out) {
     return copysignf(cap_out * fmaf(-2.f, r, 1.f), u);
 }
 
-// Number of entries < key (strict) or <= key in a sorted array of 128.
-template <bool STRICT>
-__device__ __forceinline__ int count_below(const volatile int* a, int key) {
-    int pos = 0;
+// In a non-decreasing array of 128 ids: below = #{a < key}, upto = #{a <= key}.
+// Two rounds of independent loads: the last id of each 16-id block says how
+// many whole blocks lie below the key, then the one block that holds the
+// boundary is counted (four 16-byte loads).
+__device__ __forceinline__ void seg_bounds(const int* a, int key, int& below, int& upto) {
+    int bl = 0, bu = 0;
 #pragma unroll
-    for (int step = 64; step >= 1; step >>= 1) {
-        const int v = a[pos + step - 1];
-        if (STRICT ? (v < key) : (v <= key)) pos += step;
+    for (int q = 0; q < 8; ++q) {
+        const int v = a[16 * q + 15];
+        bl += v < key;
+        bu += v <= key;
     }
-    // the seven halvings settle on 0..127; a[127] itself is still open
-    const int v = a[pos];
-    if (pos == 127 && (STRICT ? (v < key) : (v <= key))) pos = 128;
-    return pos;
+    const int4* blo = reinterpret_cast<const int4*>(a + 16 * min(bl, 7));
+    const int4* bup = reinterpret_cast<const int4*>(a + 16 * min(bu, 7));
+    int cl = 0, cu = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int4 vl = blo[q], vu = bup[q];
+        cl += (vl.x < key) + (vl.y < key) + (vl.z < key) + (vl.w < key);
+        cu += (vu.x <= key) + (vu.y <= key) + (vu.z <= key) + (vu.w <= key);
+    }
+    below = bl < 8 ? 16 * bl + cl : 128;
+    upto = bu < 8 ? 16 * bu + cu : 128;
 }
 
 // One pair of probabilities: p = 2^(x * sc - m), by MUFU or by polynomial.
@@ -728,11 +738,12 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 int seg_lo = 0, seg_hi = -1;
                 if (partial && doc) {
                     // the tile's segment ids into shared memory (one per
-                    // thread), then each row's visible columns by binary
-                    // search.  B_SEG + t counts the tile's 4 warps (each
-                    // arrives once its 32 ids are written); the buffer
-                    // alternates, and a warp reaching document tile d+2 has
-                    // seen every warp arrive at d+1, i.e. finish with d.
+                    // thread), then each row's visible columns by counting
+                    // the ids below and up to its own (seg_bounds).  B_SEG + t
+                    // counts the tile's 4 warps (each arrives once its 32 ids
+                    // are written); the buffer alternates, and a warp reaching
+                    // document tile d+2 has seen every warp arrive at d+1,
+                    // i.e. finish with d.
                     const uint32_t ph = doc_tiles & 1;
                     ++doc_tiles;
                     int* buf = seg_tile + ph * 128;
@@ -743,8 +754,9 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     const int kp = rs.next_part();
                     seg_next = (kp >= 0 && kp * kBlock + r < p.kv_len) ? __ldg(seg_row + kp * kBlock + r) : INT_MAX;
                     if (!mbar_wait_warp(bar(B_SEG + t), ph, wc, S_SEG)) { ok = false; break; }
-                    seg_lo = count_below<true>(buf, my_seg);
-                    seg_hi = count_below<false>(buf, my_seg) - 1;
+                    int upto;
+                    seg_bounds(buf, my_seg, seg_lo, upto);
+                    seg_hi = upto - 1;
                 }
                 // The tile's two 64-column halves, each in its own S buffer:
                 // while this warpgroup works on one, the tensor pipe fills
@@ -800,8 +812,8 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     } else if (SCORE == FA_SCORE_ALIBI) {
                         // bias -slope |i - j|; when every (row, column) pair of
                         // the warp's rows and the half's columns lies on one side
-                        // of the diagonal it is affine in the column and takes one
-                        // packed FMA per pair.
+                        // of the diagonal it is affine in the column: two packed
+                        // FMAs per pair.
                         const float di = static_cast<float>(i - ch);
                         const int wrow0 = qb * kBlock + wq * 32 - ch;     // i - ch of lane 0
                         if (wrow0 - 63 >= 0 || wrow0 + 31 <= 0) {
@@ -831,7 +843,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     // causal [0, i], window [i - W, i], prefix-LM
                     // [0, max(i, P - 1)], and for a document mask (ids
                     // non-decreasing) the columns whose id equals the row's
-                    // (found above by binary search in the tile's ids).
+                    // (found above by counting in the tile's ids).
                     if (partial) {
                         int lo = -ch, hi = p.kv_len - 1 - ch;
                         if (doc) {
@@ -845,8 +857,20 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         } else if (p.mask.kind == FA_MASK_PREFIX_LM) {
                             hi = min(hi, max(i, p.mask.prefix_len - 1) - ch);
                         }
+                        // warp-uniform shortcuts when no lane clips on one side
+                        const float off = -CUDART_INF_F;
+                        const bool clip_lo = __any_sync(0xffffffffu, lo > 0);
+                        const bool clip_hi = __any_sync(0xffffffffu, hi < 63);
+                        if (clip_lo && clip_hi) {
 #pragma unroll
-                        for (int e = 0; e < 64; ++e) x[e] = (e >= lo && e <= hi) ? x[e] : -CUDART_INF_F;
+                            for (int e = 0; e < 64; ++e) x[e] = (e >= lo && e <= hi) ? x[e] : off;
+                        } else if (clip_hi) {
+#pragma unroll
+                            for (int e = 0; e < 64; ++e) x[e] = e <= hi ? x[e] : off;
+                        } else if (clip_lo) {
+#pragma unroll
+                            for (int e = 0; e < 64; ++e) x[e] = e >= lo ? x[e] : off;
+                        }
                     }
 
                     // row max: four independent chains of 3-input max
