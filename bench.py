@@ -343,6 +343,76 @@ def summarize(w, r, step_ms, fwd_ms, peaks, peak_src):
     return out
 
 
+# ------------------------------------------------------- split-KV decoding path
+
+def decode_bytes(w):
+    """Algorithmic HBM bytes of one decoding forward with every key visible:
+    K and V once per (b, kv head), Q and O (bf16) and lse once."""
+    kv = 2 * w.B * w.Hkv * w.T * w.D * 2
+    qo = 2 * w.B * w.Hq * w.Tq * w.D * 2
+    return kv + qo + w.B * w.Hq * w.Tq * 4
+
+
+def decode_section(device, flush, steps, warmup, peaks, peak_src):
+    """Time fa_fwd_decode (split kernel + combine kernel, one CUDA graph
+    replay, L2 flushed before each) on each decoding workload."""
+    import torch
+    from block_sparse_attention_fa_gb300 import fa
+    out = {}
+    for name, w in synth.DECODE_WORKLOADS.items():
+        q, k, v = (torch.from_numpy(x).to(device).to(torch.bfloat16) for x in w.qkv())
+        bm = fa.block_mask(w.mask, 1, 1, w.Tq, w.T, window=w.window, prefix_len=w.prefix_len)
+        splits = fa.decode_splits(q, k, bm)
+        parts = fa.decode_partials(q, splits)
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.Hq, w.Tq), dtype=torch.float32, device=device)
+        ws = fa.Workspace(device)
+
+        def fn():
+            fa.fwd_decode(q, k, v, bm, num_splits=splits, out=o, lse=lse, partials=parts, workspace=ws)
+
+        side = torch.cuda.Stream(device=device)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            fn()
+            fn()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        ws.check()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        stream = torch.cuda.current_stream()
+        for _ in range(warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for a, c in evs:
+            flush.zero_()
+            a.record(stream)
+            g.replay()
+            c.record(stream)
+        torch.cuda.synchronize()
+        ws.check()
+        ms = statistics.mean(a.elapsed_time(c) for a, c in evs)
+        nbytes = decode_bytes(w)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[name] = {
+            "config": {"B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "q_len": w.Tq, "kv_len": w.T, "D": w.D,
+                       "mask": w.mask, "score": w.score, "splits": splits,
+                       "rows_per_group": (w.Hq // w.Hkv) * w.Tq},
+            "ms": round(ms, 4),
+            "tokens_per_s": round(w.B * w.Tq / (ms * 1e-3), 1),
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_source": peak_src,
+                         "kernels": ["decode_split_kernel", "decode_combine_kernel"],
+                         "algorithmic_bytes": nbytes},
+        }
+        del q, k, v, parts, o, lse
+        torch.cuda.empty_cache()
+    return out
+
+
 # ----------------------------------------------------------- CPU (oracle) side
 
 def oracle_rate(w, seconds, threads, seed=0, max_rows=None):
@@ -459,6 +529,7 @@ def main():
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -530,6 +601,10 @@ def main():
             del r2
             torch.cuda.empty_cache()
 
+    decode = None
+    if rank == 0 and not args.no_decode:
+        decode = decode_section(device, flush, args.steps, args.warmup, peaks, peak_src)
+
     cpu = None
     if rank == 0 and not args.no_cpu:
         cpu = cpu_baseline(w, r.flops, args.cpu_seconds)
@@ -565,6 +640,7 @@ def main():
             "clocks": clk.summary(),
             "peaks": {"source": peak_src, **peaks},
             "workloads": secondary,
+            "decode": decode,
             **extra,
         }
         print(json.dumps(line), flush=True)

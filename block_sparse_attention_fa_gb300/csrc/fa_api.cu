@@ -4,6 +4,7 @@
 // Every entry point validates synchronously and launches nothing when an
 // argument is rejected; unsupported requests are errors, never a silent
 // fallback to another code path.
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -129,6 +130,87 @@ fa_status make_tmap(CUtensorMap* map, const void* base, int B, int H, int T, int
     return FA_OK;
 }
 
+// Checks shared by fa_fwd and fa_fwd_decode: the arguments, the BlockMask
+// against them, and the score_mod (NULL becomes FA_SCORE_NONE in `*out`).
+fa_status check_fwd_args(const fa_fwd_args* a, const fa_block_mask* bm, void* workspace) {
+    if (!a) return fail(FA_ERR_INVALID_ARG, "fwd args are NULL");
+    if (a->dtype != FA_BF16 && a->dtype != FA_FP32) return fail(FA_ERR_INVALID_ARG, "unknown dtype %d", a->dtype);
+    if (a->B < 1 || a->Hq < 1 || a->Hkv < 1 || a->q_len < 1 || a->kv_len < 1)
+        return fail(FA_ERR_INVALID_ARG, "extents must be >= 1 (B=%d Hq=%d Hkv=%d q_len=%d kv_len=%d)", a->B,
+                    a->Hq, a->Hkv, a->q_len, a->kv_len);
+    if (a->Hq % a->Hkv != 0)
+        return fail(FA_ERR_INVALID_ARG, "Hq (%d) must be a multiple of Hkv (%d)", a->Hq, a->Hkv);
+    if (a->D != 64 && a->D != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d not supported (64 or 128)", a->D);
+    if (!a->q || !a->k || !a->v || !a->o || !a->lse)
+        return fail(FA_ERR_INVALID_ARG, "q, k, v, o and lse must be non-NULL");
+    if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v) || !aligned16(a->o) ||
+        (reinterpret_cast<uintptr_t>(a->lse) & 3u))
+        return fail(FA_ERR_INVALID_ARG, "q, k, v, o must be 16-byte aligned and lse 4-byte aligned");
+    if (!(std::isfinite(a->scale))) return fail(FA_ERR_INVALID_ARG, "scale must be finite");
+    if (!workspace) return fail(FA_ERR_INVALID_ARG, "workspace is NULL");
+    if (a->flags & ~FA_OUT_FP32) return fail(FA_ERR_INVALID_ARG, "unknown flags 0x%x", a->flags);
+    if ((a->flags & FA_OUT_FP32) && a->dtype != FA_BF16)
+        return fail(FA_ERR_INVALID_ARG, "FA_OUT_FP32 applies to bf16 inputs only");
+    if (a->debug_flags & ~FA_DEBUG_DROP_FIRST_LOAD)
+        return fail(FA_ERR_INVALID_ARG, "unknown debug flags 0x%x", a->debug_flags);
+    fa_status st = check_block_mask(bm);
+    if (st != FA_OK) return st;
+    if (bm->q_len != a->q_len || bm->kv_len != a->kv_len)
+        return fail(FA_ERR_INVALID_ARG, "block mask was built for (%d, %d), not (%d, %d)", bm->q_len, bm->kv_len,
+                    a->q_len, a->kv_len);
+    if (bm->B != 1 && bm->B != a->B) return fail(FA_ERR_INVALID_ARG, "block mask B=%d must be 1 or %d", bm->B, a->B);
+    if (bm->H != 1 && bm->H != a->Hq)
+        return fail(FA_ERR_INVALID_ARG, "block mask H=%d must be 1 or %d", bm->H, a->Hq);
+    if (bm->mask.kind == FA_MASK_DOCUMENT && bm->mask.seg_batch != 1 && bm->mask.seg_batch != a->B)
+        return fail(FA_ERR_INVALID_ARG, "seg_batch must be 1 or B=%d", a->B);
+    return FA_OK;
+}
+
+fa_status check_score(const fa_score_desc* sc, fa_score_desc* out) {
+    if (!sc) {
+        *out = fa_score_desc{};
+        out->kind = FA_SCORE_NONE;
+        return FA_OK;
+    }
+    switch (sc->kind) {
+        case FA_SCORE_NONE: break;
+        case FA_SCORE_SOFTCAP:
+            if (!(sc->softcap > 0.f) || !std::isfinite(sc->softcap))
+                return fail(FA_ERR_INVALID_ARG, "softcap must be finite and > 0");
+            break;
+        case FA_SCORE_ALIBI:
+            if (!sc->alibi_slopes) return fail(FA_ERR_INVALID_ARG, "ALiBi needs alibi_slopes");
+            break;
+        case FA_SCORE_REL_BIAS:
+            if (!sc->rel_bias || sc->rel_max < 0) return fail(FA_ERR_INVALID_ARG, "relative bias needs rel_bias and rel_max >= 0");
+            break;
+        default: return fail(FA_ERR_INVALID_ARG, "unknown score kind %d", sc->kind);
+    }
+    *out = *sc;
+    return FA_OK;
+}
+
+// Streaming multiprocessors of the current device (cached per device).
+int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+    if (dev < 64 && cached[dev] > 0) return cached[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 148;
+    if (dev < 64) cached[dev] = n;
+    return n;
+}
+
+// Rows of one decode row group, and whether a row group holds all query
+// heads of a kv head (the BlockMask row is shared by the heads).
+void decode_shape(const fa_fwd_args* a, const fa_block_mask* bm, int* rows, int* grouped, int* groups) {
+    const bool g = bm->H == 1;
+    *grouped = g ? 1 : 0;
+    *rows = g ? (a->Hq / a->Hkv) * a->q_len : a->q_len;
+    *groups = a->B * (g ? a->Hkv : a->Hq);
+}
+
 }  // namespace
 
 fa_status fa::report(fa_status st, const char* msg) {
@@ -179,56 +261,13 @@ fa_status fa_block_mask_build(const fa_block_mask* bm, void* workspace, void* st
 
 fa_status fa_fwd(const fa_fwd_args* a, const fa_block_mask* bm, const fa_score_desc* sc, void* workspace,
                  void* stream) {
-    if (!a) return fail(FA_ERR_INVALID_ARG, "fwd args are NULL");
-    if (a->dtype != FA_BF16 && a->dtype != FA_FP32) return fail(FA_ERR_INVALID_ARG, "unknown dtype %d", a->dtype);
-    if (a->B < 1 || a->Hq < 1 || a->Hkv < 1 || a->q_len < 1 || a->kv_len < 1)
-        return fail(FA_ERR_INVALID_ARG, "extents must be >= 1 (B=%d Hq=%d Hkv=%d q_len=%d kv_len=%d)", a->B,
-                    a->Hq, a->Hkv, a->q_len, a->kv_len);
-    if (a->Hq % a->Hkv != 0)
-        return fail(FA_ERR_INVALID_ARG, "Hq (%d) must be a multiple of Hkv (%d)", a->Hq, a->Hkv);
-    if (a->D != 64 && a->D != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d not supported (64 or 128)", a->D);
-    if (!a->q || !a->k || !a->v || !a->o || !a->lse)
-        return fail(FA_ERR_INVALID_ARG, "q, k, v, o and lse must be non-NULL");
-    if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v) || !aligned16(a->o) ||
-        (reinterpret_cast<uintptr_t>(a->lse) & 3u))
-        return fail(FA_ERR_INVALID_ARG, "q, k, v, o must be 16-byte aligned and lse 4-byte aligned");
-    if (!(std::isfinite(a->scale))) return fail(FA_ERR_INVALID_ARG, "scale must be finite");
-    if (!workspace) return fail(FA_ERR_INVALID_ARG, "workspace is NULL");
-    if (a->flags & ~FA_OUT_FP32) return fail(FA_ERR_INVALID_ARG, "unknown flags 0x%x", a->flags);
-    if ((a->flags & FA_OUT_FP32) && a->dtype != FA_BF16)
-        return fail(FA_ERR_INVALID_ARG, "FA_OUT_FP32 applies to bf16 inputs only");
-    if (a->debug_flags & ~FA_DEBUG_DROP_FIRST_LOAD)
-        return fail(FA_ERR_INVALID_ARG, "unknown debug flags 0x%x", a->debug_flags);
-    fa_status st = check_block_mask(bm);
+    fa_status st = check_fwd_args(a, bm, workspace);
     if (st != FA_OK) return st;
-    if (bm->q_len != a->q_len || bm->kv_len != a->kv_len)
-        return fail(FA_ERR_INVALID_ARG, "block mask was built for (%d, %d), not (%d, %d)", bm->q_len, bm->kv_len,
-                    a->q_len, a->kv_len);
-    if (bm->B != 1 && bm->B != a->B) return fail(FA_ERR_INVALID_ARG, "block mask B=%d must be 1 or %d", bm->B, a->B);
-    if (bm->H != 1 && bm->H != a->Hq)
-        return fail(FA_ERR_INVALID_ARG, "block mask H=%d must be 1 or %d", bm->H, a->Hq);
-    if (bm->mask.kind == FA_MASK_DOCUMENT && bm->mask.seg_batch != 1 && bm->mask.seg_batch != a->B)
-        return fail(FA_ERR_INVALID_ARG, "seg_batch must be 1 or B=%d", a->B);
     const long long units = (long long)a->B * a->Hq * bm->nq;
     if (units * 2 > 2147483647LL) return fail(FA_ERR_UNSUPPORTED, "too many work units (%lld)", units);
-
-    fa_score_desc none{};
-    none.kind = FA_SCORE_NONE;
-    if (!sc) sc = &none;
-    switch (sc->kind) {
-        case FA_SCORE_NONE: break;
-        case FA_SCORE_SOFTCAP:
-            if (!(sc->softcap > 0.f) || !std::isfinite(sc->softcap))
-                return fail(FA_ERR_INVALID_ARG, "softcap must be finite and > 0");
-            break;
-        case FA_SCORE_ALIBI:
-            if (!sc->alibi_slopes) return fail(FA_ERR_INVALID_ARG, "ALiBi needs alibi_slopes");
-            break;
-        case FA_SCORE_REL_BIAS:
-            if (!sc->rel_bias || sc->rel_max < 0) return fail(FA_ERR_INVALID_ARG, "relative bias needs rel_bias and rel_max >= 0");
-            break;
-        default: return fail(FA_ERR_INVALID_ARG, "unknown score kind %d", sc->kind);
-    }
+    fa_score_desc score;
+    if ((st = check_score(sc, &score)) != FA_OK) return st;
+    sc = &score;
 
     fa::FwdParams p{};
     p.B = a->B;
@@ -266,6 +305,91 @@ fa_status fa_fwd(const fa_fwd_args* a, const fa_block_mask* bm, const fa_score_d
         e = fa::launch_fwd_bf16(p, tq, tk, tv, s);
     }
     if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+    return ok();
+}
+
+size_t fa_decode_partials_bytes(const fa_fwd_args* a, int32_t num_splits) {
+    if (!a || a->B < 1 || a->Hq < 1 || a->q_len < 1 || (a->D != 64 && a->D != 128) || num_splits < 1) return 0;
+    return (size_t)a->B * a->Hq * a->q_len * num_splits * (a->D + 2) * sizeof(float);
+}
+
+int32_t fa_decode_splits(const fa_fwd_args* a, const fa_block_mask* bm) {
+    if (!a || !bm || a->B < 1 || a->Hkv < 1 || a->Hq < 1 || bm->nkv < 1 || (bm->H != 1 && bm->H != a->Hq)) return 0;
+    int rows, grouped, groups;
+    decode_shape(a, bm, &rows, &grouped, &groups);
+    // One CTA per SM: the fewest waves times tiles per split, counting every
+    // kv tile of the row (the visited count lives on the device).
+    const int sms = sm_count();
+    const int cap = std::min(bm->nkv, fa::decode_max_splits());
+    long long best = -1;
+    int best_s = 1;
+    for (int sp = 1; sp <= cap; ++sp) {
+        const long long waves = ((long long)groups * sp + sms - 1) / sms;
+        const long long cost = waves * ((bm->nkv + sp - 1) / sp);
+        if (best < 0 || cost < best) {
+            best = cost;
+            best_s = sp;
+        }
+    }
+    return best_s;
+}
+
+fa_status fa_fwd_decode(const fa_fwd_args* a, const fa_block_mask* bm, const fa_score_desc* sc, int32_t num_splits,
+                        float* partials, size_t partials_bytes, void* workspace, void* stream) {
+    fa_status st = check_fwd_args(a, bm, workspace);
+    if (st != FA_OK) return st;
+    fa_score_desc score;
+    if ((st = check_score(sc, &score)) != FA_OK) return st;
+    if (a->dtype != FA_BF16) return fail(FA_ERR_UNSUPPORTED, "the decoding forward takes bf16 inputs");
+    if (a->debug_flags) return fail(FA_ERR_UNSUPPORTED, "the decoding forward takes no debug flags");
+    if (bm->nq != 1) return fail(FA_ERR_UNSUPPORTED, "the decoding forward takes q_len <= 128 (got %d)", a->q_len);
+    if (bm->mask.kind == FA_MASK_DOCUMENT)
+        return fail(FA_ERR_UNSUPPORTED, "the decoding forward does not take document masks");
+    int rows, grouped, groups;
+    decode_shape(a, bm, &rows, &grouped, &groups);
+    if (rows > fa::decode_max_rows())
+        return fail(FA_ERR_UNSUPPORTED, "the decoding forward takes at most %d query rows per %s (got %d)",
+                    fa::decode_max_rows(), grouped ? "kv head" : "query head", rows);
+    if (num_splits == 0) num_splits = fa_decode_splits(a, bm);
+    if (num_splits < 1 || num_splits > fa::decode_max_splits())
+        return fail(FA_ERR_INVALID_ARG, "num_splits must be in [1, %d] or 0 (got %d)", fa::decode_max_splits(),
+                    num_splits);
+    if (groups > 65535) return fail(FA_ERR_UNSUPPORTED, "too many row groups (%d)", groups);
+    const size_t need = fa_decode_partials_bytes(a, num_splits);
+    if (!partials || !aligned16(partials))
+        return fail(FA_ERR_INVALID_ARG, "partials must be non-NULL and 16-byte aligned");
+    if (partials_bytes < need)
+        return fail(FA_ERR_INVALID_ARG, "partials hold %zu bytes, %zu needed", partials_bytes, need);
+
+    fa::DecodeParams p{};
+    p.B = a->B;
+    p.Hq = a->Hq;
+    p.Hkv = a->Hkv;
+    p.q_len = a->q_len;
+    p.kv_len = a->kv_len;
+    p.D = a->D;
+    p.group = a->Hq / a->Hkv;
+    p.rows = rows;
+    p.grouped = grouped;
+    p.num_groups = groups;
+    p.splits = num_splits;
+    p.scale = a->scale > 0.f ? a->scale : 1.0f / std::sqrt((float)a->D);
+    p.bm = {bm->B, bm->H, bm->nq, bm->nkv, bm->kv_num_blocks, bm->kv_indices, bm->full_kv_num_blocks,
+            bm->full_kv_indices};
+    p.mask = mask_params(bm);
+    p.score = {score.kind, score.softcap, score.alibi_slopes, score.rel_bias, score.rel_max};
+    p.q = a->q;
+    p.o = a->o;
+    p.lse = a->lse;
+    p.partials = partials;
+    p.ws = static_cast<uint32_t*>(workspace);
+    p.timeout_ns = (uint64_t)(a->timeout_ms ? a->timeout_ms : 2000u) * 1000000ull;
+    p.flags = a->flags;
+    alignas(64) CUtensorMap tk, tv;
+    if ((st = make_tmap(&tk, a->k, a->B, a->Hkv, a->kv_len, a->D)) != FA_OK) return st;
+    if ((st = make_tmap(&tv, a->v, a->B, a->Hkv, a->kv_len, a->D)) != FA_OK) return st;
+    cudaError_t e = fa::launch_decode_bf16(p, tk, tv, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     return ok();
 }
 

@@ -58,6 +58,26 @@ struct FwdParams {
     uint32_t debug_flags;
 };
 
+// The split-KV decoding forward (decode_bf16.cu).
+struct DecodeParams {
+    int B, Hq, Hkv, q_len, kv_len, D, group;
+    int rows;                     // query rows per row group (<= 16)
+    int grouped;                  // 1: a row group is (b, kv head), all its query heads; 0: (b, query head)
+    int num_groups;               // B * Hkv or B * Hq
+    int splits;                   // kv splits per row group
+    float scale;
+    BlockMaskView bm;
+    MaskParams mask;
+    ScoreParams score;
+    const void* q;
+    void* o;
+    float* lse;
+    float* partials;              // [B][Hq][q_len][splits][D + 2]: O, m, l of each split
+    uint32_t* ws;
+    uint64_t timeout_ns;
+    uint32_t flags;
+};
+
 struct BuildParams {
     int B, H, q_len, kv_len, nq, nkv;
     MaskParams mask;
@@ -76,5 +96,9 @@ cudaError_t launch_block_mask_build(const BuildParams& p, cudaStream_t s);
 cudaError_t launch_fwd_fp32(const FwdParams& p, cudaStream_t s);
 cudaError_t launch_fwd_bf16(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, cudaStream_t s);
+cudaError_t launch_decode_bf16(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                               cudaStream_t s);
+int decode_max_splits();
+int decode_max_rows();
 
 }  // namespace fa

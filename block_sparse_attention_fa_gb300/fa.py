@@ -25,7 +25,8 @@ DEBUG_DROP_FIRST_LOAD = 1
 BLOCK = 128
 
 SYMBOLS = ("fa_workspace_bytes", "fa_block_mask_shape", "fa_block_mask_build", "fa_fwd",
-           "fa_fwd_noalloc", "fa_workspace_check", "fa_last_error", "fa_version")
+           "fa_fwd_noalloc", "fa_fwd_decode", "fa_decode_partials_bytes", "fa_decode_splits",
+           "fa_workspace_check", "fa_last_error", "fa_version")
 
 
 class FAError(RuntimeError):
@@ -88,6 +89,14 @@ def load_library(path: str = LIB_PATH):
     h.fa_fwd_noalloc.restype = ctypes.c_int
     h.fa_fwd_noalloc.argtypes = [ctypes.POINTER(FwdArgs), ctypes.POINTER(BlockMaskStruct),
                                  ctypes.POINTER(ScoreDesc), ctypes.c_void_p]
+    h.fa_fwd_decode.restype = ctypes.c_int
+    h.fa_fwd_decode.argtypes = [ctypes.POINTER(FwdArgs), ctypes.POINTER(BlockMaskStruct),
+                                ctypes.POINTER(ScoreDesc), ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t,
+                                ctypes.c_void_p, ctypes.c_void_p]
+    h.fa_decode_partials_bytes.restype = ctypes.c_size_t
+    h.fa_decode_partials_bytes.argtypes = [ctypes.POINTER(FwdArgs), ctypes.c_int32]
+    h.fa_decode_splits.restype = ctypes.c_int32
+    h.fa_decode_splits.argtypes = [ctypes.POINTER(FwdArgs), ctypes.POINTER(BlockMaskStruct)]
     h.fa_workspace_check.restype = ctypes.c_int
     h.fa_workspace_check.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
     h.fa_last_error.restype = ctypes.c_char_p
@@ -284,6 +293,77 @@ def fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, bm: BlockMask
         sc.rel_max = rel_max
     _check(load_library().fa_fwd_noalloc(ctypes.byref(a), ctypes.byref(bm.struct), ctypes.byref(sc),
                                          _stream_ptr(stream)))
+    return out, lse
+
+
+def _score_desc(score, softcap, alibi_slopes, rel_bias, rel_max) -> ScoreDesc:
+    sc = ScoreDesc()
+    sc.kind = SCORE_KINDS[score]
+    sc.softcap = softcap
+    if alibi_slopes is not None:
+        sc.alibi_slopes = alibi_slopes.data_ptr()
+    if rel_bias is not None:
+        sc.rel_bias = rel_bias.data_ptr()
+        sc.rel_max = rel_max
+    return sc
+
+
+def decode_args(q: torch.Tensor, k: torch.Tensor, out: torch.Tensor, lse: torch.Tensor, v: torch.Tensor = None,
+                scale: Optional[float] = None, out_fp32: bool = False) -> FwdArgs:
+    """The fa_fwd_args of a bf16 decoding call (shapes taken from q and k)."""
+    B, Hq, Tq, D = q.shape
+    a = FwdArgs()
+    a.dtype, a.B, a.Hq, a.Hkv, a.q_len, a.kv_len, a.D = BF16, B, Hq, k.shape[1], Tq, k.shape[2], D
+    a.scale = 0.0 if scale is None else float(scale)
+    a.q, a.k, a.o, a.lse = q.data_ptr(), k.data_ptr(), out.data_ptr(), lse.data_ptr()
+    a.v = (v if v is not None else k).data_ptr()
+    a.flags = OUT_FP32 if out_fp32 else 0
+    return a
+
+
+def decode_splits(q: torch.Tensor, k: torch.Tensor, bm: BlockMask) -> int:
+    """The split count fa_fwd_decode picks for num_splits=0 on this device."""
+    a = decode_args(q, k, q, q)
+    return int(load_library().fa_decode_splits(ctypes.byref(a), ctypes.byref(bm.struct)))
+
+
+def decode_partials(q: torch.Tensor, num_splits: int) -> torch.Tensor:
+    """fp32 scratch for fa_fwd_decode: [B, Hq, q_len, num_splits, D + 2]."""
+    B, Hq, Tq, D = q.shape
+    return torch.empty((B, Hq, Tq, num_splits, D + 2), dtype=torch.float32, device=q.device)
+
+
+def fwd_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, bm: BlockMask, *, score: str = "none",
+               softcap: float = 0.0, alibi_slopes: Optional[torch.Tensor] = None,
+               rel_bias: Optional[torch.Tensor] = None, rel_max: int = 0, scale: Optional[float] = None,
+               num_splits: int = 0, out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+               partials: Optional[torch.Tensor] = None, workspace: Optional[Workspace] = None, stream=None,
+               timeout_ms: int = 0, out_fp32: bool = False):
+    """Split-KV decoding forward (fa_fwd_decode) for bf16 q of at most 128
+    rows; returns (o, lse).  ``num_splits`` 0 lets the library choose;
+    ``partials`` (see decode_partials) is allocated when not given."""
+    if q.dtype != torch.bfloat16 or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("fwd_decode takes bf16 q, k, v")
+    for t in (q, k, v):
+        if not (t.is_cuda and t.is_contiguous() and t.dim() == 4):
+            raise ValueError("q, k, v must be contiguous CUDA tensors [B, H, T, D]")
+    B, Hq, Tq, D = q.shape
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.float32 if out_fp32 else q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq, Tq), dtype=torch.float32, device=q.device)
+    a = decode_args(q, k, out, lse, v=v, scale=scale, out_fp32=out_fp32)
+    a.timeout_ms = timeout_ms
+    lib = load_library()
+    if num_splits == 0:
+        num_splits = int(lib.fa_decode_splits(ctypes.byref(a), ctypes.byref(bm.struct))) or 1
+    if partials is None:
+        partials = decode_partials(q, num_splits)
+    sc = _score_desc(score, softcap, alibi_slopes, rel_bias, rel_max)
+    ws = workspace or default_workspace(q.device, stream)
+    _check(lib.fa_fwd_decode(ctypes.byref(a), ctypes.byref(bm.struct), ctypes.byref(sc), num_splits,
+                             ctypes.c_void_p(partials.data_ptr()), partials.numel() * partials.element_size(),
+                             ws.ptr, _stream_ptr(stream)))
     return out, lse
 
 

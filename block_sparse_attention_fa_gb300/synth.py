@@ -112,6 +112,11 @@ class Workload:
     input_scale: float = 1.0
     seed: int = 0
     groups: Optional[int] = None   # number of independent windows (grouped workloads)
+    q_len: Optional[int] = None    # query rows when they differ from T (decoding shapes)
+
+    @property
+    def Tq(self) -> int:
+        return self.q_len or self.T
 
     @property
     def kv_len(self) -> int:
@@ -136,7 +141,7 @@ class Workload:
 
     def qkv(self):
         """(q, k, v) fp32 numpy arrays; bf16 workloads are pre-rounded to bf16."""
-        q = standard_normal(self.seed * 3 + 0, (self.B, self.Hq, self.T, self.D), self.input_scale)
+        q = standard_normal(self.seed * 3 + 0, (self.B, self.Hq, self.Tq, self.D), self.input_scale)
         k = standard_normal(self.seed * 3 + 1, (self.B, self.Hkv, self.T, self.D), self.input_scale)
         v = standard_normal(self.seed * 3 + 2, (self.B, self.Hkv, self.T, self.D), self.input_scale)
         if self.dtype == "bf16":
@@ -147,6 +152,18 @@ class Workload:
         """A copy with some fields replaced (for downscaled parity cases)."""
         return dataclasses.replace(self, **kw)
 
+
+# Decoding shapes for the split-KV forward (fa_fwd_decode): a few query rows
+# per (batch, query head) against a long key/value sequence; every key
+# visible.  GQA 32 / 8 and T = 32768 as the window workload.
+DECODE_WORKLOADS = {
+    "decode_gqa_bf16": Workload(
+        name="decode_gqa_bf16", dtype="bf16", B=8, Hq=32, Hkv=8, T=32768, D=128,
+        mask="full", seed=6, q_len=1),
+    "decode_spec4_bf16": Workload(
+        name="decode_spec4_bf16", dtype="bf16", B=8, Hq=32, Hkv=8, T=32768, D=128,
+        mask="full", seed=7, q_len=4),
+}
 
 WORKLOADS = {
     "grouped_fp32": Workload(

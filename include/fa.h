@@ -208,6 +208,40 @@ fa_status fa_fwd(const fa_fwd_args *a, const fa_block_mask *bm, const fa_score_d
 fa_status fa_fwd_noalloc(const fa_fwd_args *a, const fa_block_mask *bm, const fa_score_desc *sc,
                          void *stream);
 
+/* Split-KV decoding forward: the same result as fa_fwd for a few query rows
+ * against a long key/value sequence.  FlexAttention pairs its prefill kernel
+ * with a decoding kernel (FlexAttention wiki page, "Development history": the
+ * FlexDecoding backend for long-context decoding; "Core technology":
+ * flex_decoding beside flex_attention); this is that shape.  The visited kv
+ * tiles of each row group are split into `num_splits` parts, one CTA each,
+ * and a second launch merges the parts' (O, max, sum) per row.
+ *   A row group is the query rows that share one K/V stream and one BlockMask
+ *   row: with a BlockMask of H = 1, all Hq / Hkv query heads x q_len rows of
+ *   a (batch, kv head); with H = Hq, the q_len rows of a (batch, query head).
+ *   Requirements beyond fa_fwd's (else FA_ERR_UNSUPPORTED): bf16 inputs,
+ *   q_len <= 128 (one q-block), at most 16 rows per row group, no document
+ *   mask, no debug flags.
+ *   num_splits  1 .. 256, or 0 for fa_decode_splits(a, bm).
+ *   partials    caller-owned device fp32 scratch of at least
+ *               fa_decode_partials_bytes(a, num_splits) bytes, 16-byte
+ *               aligned: [B][Hq][q_len][num_splits][D + 2] (each split's
+ *               unnormalised O, then its running max and sum, base 2).
+ *               Overwritten by every call; calls that may overlap need their
+ *               own.
+ * Two kernel launches, asynchronous on `stream`.                            */
+fa_status fa_fwd_decode(const fa_fwd_args *a, const fa_block_mask *bm, const fa_score_desc *sc,
+                        int32_t num_splits, float *partials, size_t partials_bytes, void *workspace,
+                        void *stream);
+
+/* Bytes of `partials` fa_fwd_decode needs for these arguments and split
+ * count (0 if the arguments cannot be valid).                               */
+size_t fa_decode_partials_bytes(const fa_fwd_args *a, int32_t num_splits);
+
+/* The split count fa_fwd_decode uses for num_splits = 0: with one CTA per
+ * SM of the current device, the count that minimises waves x tiles per split
+ * over the row's nkv tiles (0 if the arguments cannot be valid).            */
+int32_t fa_decode_splits(const fa_fwd_args *a, const fa_block_mask *bm);
+
 /* Synchronise `stream`, then report and clear the device-side flags in
  * `workspace`: FA_OK, FA_ERR_TIMEOUT or FA_ERR_DEVICE_CHECK (details in
  * fa_last_error()), or FA_ERR_CUDA if the stream itself reports an error.  */

@@ -31,8 +31,9 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted([
-        "fa_block_mask_build", "fa_block_mask_shape", "fa_fwd", "fa_fwd_noalloc", "fa_last_error", "fa_version",
-        "fa_workspace_bytes", "fa_workspace_check"])
+        "fa_block_mask_build", "fa_block_mask_shape", "fa_decode_partials_bytes", "fa_decode_splits", "fa_fwd",
+        "fa_fwd_decode", "fa_fwd_noalloc", "fa_last_error", "fa_version", "fa_workspace_bytes",
+        "fa_workspace_check"])
 
 
 def test_library_exports_every_declared_symbol(fa):
@@ -175,3 +176,58 @@ def test_fwd_rejects_null_args(fa):
     a = _args(fa)
     assert lib.fa_fwd(ctypes.byref(a), ctypes.byref(_bm(fa)), None, None, None) == fa.ERR_INVALID_ARG
     assert b"workspace" in lib.fa_last_error()
+
+
+def _partials_ok(fa, a, splits):
+    return fa.load_library().fa_decode_partials_bytes(ctypes.byref(a), splits)
+
+
+@pytest.mark.parametrize("kw,bmkw,splits,status,text", [
+    ({"dtype": 1}, {}, 1, "ERR_UNSUPPORTED", b"bf16"),
+    ({}, {}, 1, "ERR_UNSUPPORTED", b"q_len <= 128"),
+    ({"q_len": 1, "kv_len": 1}, {"q_len": 1, "nq": 1, "mask_kind": 3, "mask_seg_ids": FAKE, "mask_seg_batch": 1,
+                    "kv_len": 1, "nkv": 1}, 1, "ERR_UNSUPPORTED", b"document"),
+    ({"q_len": 1, "Hq": 32, "Hkv": 1}, {"q_len": 1, "nq": 1}, 1, "ERR_UNSUPPORTED", b"at most 16"),
+    ({"q_len": 8, "Hq": 4, "Hkv": 1}, {"q_len": 8, "nq": 1}, 1, "ERR_UNSUPPORTED", b"at most 16"),
+    ({"q_len": 1}, {"q_len": 1, "nq": 1}, 300, "ERR_INVALID_ARG", b"num_splits"),
+    ({"q_len": 1}, {"q_len": 1, "nq": 1}, -1, "ERR_INVALID_ARG", b"num_splits"),
+    ({"q_len": 1, "debug_flags": 1}, {"q_len": 1, "nq": 1}, 1, "ERR_UNSUPPORTED", b"debug"),
+])
+def test_decode_rejects(fa, kw, bmkw, splits, status, text):
+    lib = fa.load_library()
+    a = _args(fa, **kw)
+    bm = _bm(fa, **bmkw)
+    st = lib.fa_fwd_decode(ctypes.byref(a), ctypes.byref(bm), None, splits, ctypes.c_void_p(FAKE), 1 << 40,
+                           ctypes.c_void_p(FAKE), None)
+    assert st == getattr(fa, status), lib.fa_last_error()
+    assert text in lib.fa_last_error()
+
+
+def test_decode_partials_checks(fa):
+    lib = fa.load_library()
+    a = _args(fa, q_len=2, Hq=8, Hkv=2)
+    bm = _bm(fa, q_len=2, nq=1)
+    need = lib.fa_decode_partials_bytes(ctypes.byref(a), 5)
+    assert need == 1 * 8 * 2 * 5 * (128 + 2) * 4
+    assert lib.fa_decode_partials_bytes(ctypes.byref(a), 0) == 0
+    assert lib.fa_fwd_decode(ctypes.byref(a), ctypes.byref(bm), None, 5, None, need, ctypes.c_void_p(FAKE),
+                             None) == fa.ERR_INVALID_ARG
+    assert b"partials" in lib.fa_last_error()
+    assert lib.fa_fwd_decode(ctypes.byref(a), ctypes.byref(bm), None, 5, ctypes.c_void_p(FAKE + 4), need,
+                             ctypes.c_void_p(FAKE), None) == fa.ERR_INVALID_ARG
+    assert lib.fa_fwd_decode(ctypes.byref(a), ctypes.byref(bm), None, 5, ctypes.c_void_p(FAKE), need - 4,
+                             ctypes.c_void_p(FAKE), None) == fa.ERR_INVALID_ARG
+    assert b"needed" in lib.fa_last_error()
+
+
+def test_decode_split_choice(fa):
+    """The automatic split count lies in [1, nkv] and grows with the length."""
+    lib = fa.load_library()
+    a = _args(fa, q_len=1, B=1, Hq=8, Hkv=8, kv_len=32768)
+    short = _bm(fa, q_len=1, nq=1, kv_len=256, nkv=2)
+    long_ = _bm(fa, q_len=1, nq=1, kv_len=32768, nkv=256)
+    s_short = lib.fa_decode_splits(ctypes.byref(a), ctypes.byref(short))
+    s_long = lib.fa_decode_splits(ctypes.byref(a), ctypes.byref(long_))
+    assert 1 <= s_short <= 2
+    assert s_short <= s_long <= 256
+    assert lib.fa_decode_splits(None, ctypes.byref(long_)) == 0
