@@ -26,7 +26,7 @@
 //       bound by HBM (every K/V byte is read once), not by the tensor pipe.
 //       At the end of the split the eight warp states are merged through
 //       shared memory.
-//   decode_combine_kernel one warp per query row merges the splits:
+//   decode_combine_kernel one CTA per query row merges the splits:
 //       M = max_s m_s, L = sum_s 2^(m_s - M) l_s, O = sum_s 2^(m_s - M) O_s / L,
 //       lse = (M + log2 L) ln 2; a row no split saw gets O = 0, lse = -inf.
 //
@@ -394,47 +394,57 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     }
 }
 
+// One CTA of D threads per query row; thread d owns column d of O.
 template <int D>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(D)
 decode_combine_kernel(const DecodeParams p) {
-    extern __shared__ float wts[];                 // [4 warps][splits]
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const long long row = (long long)blockIdx.x * 4 + warp;
-    const long long rows = (long long)p.B * p.Hq * p.q_len;
-    if (row >= rows) return;
+    extern __shared__ float wts[];                 // [splits]: 2^(m_s - M)
+    __shared__ float red[D / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const long long row = blockIdx.x;
     const int S = p.splits;
     const float* part = p.partials + row * S * (D + 2);
-    float* w = wts + warp * S;
     float mm = -CUDART_INF_F;
-    for (int s = lane; s < S; s += 32) mm = fmaxf(mm, part[(size_t)s * (D + 2) + D]);
+    for (int s = tid; s < S; s += D) mm = fmaxf(mm, part[(size_t)s * (D + 2) + D]);
 #pragma unroll
     for (int k = 16; k > 0; k >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, k));
+    if (lane == 0) red[warp] = mm;
+    __syncthreads();
+    mm = red[0];
+#pragma unroll
+    for (int w = 1; w < D / 32; ++w) mm = fmaxf(mm, red[w]);
+    __syncthreads();
     float ll = 0.f;
-    for (int s = lane; s < S; s += 32) {
+    for (int s = tid; s < S; s += D) {
         const float ms = part[(size_t)s * (D + 2) + D];
         const float f = (mm == -CUDART_INF_F || ms == -CUDART_INF_F) ? 0.f : ex2_approx(ms - mm);
-        w[s] = f;
+        wts[s] = f;
         ll = fmaf(part[(size_t)s * (D + 2) + D + 1], f, ll);
     }
 #pragma unroll
     for (int k = 16; k > 0; k >>= 1) ll += __shfl_xor_sync(0xffffffffu, ll, k);
-    __syncwarp();
-    const bool empty = !(ll > 0.f);
-    const float inv = empty ? 0.f : 1.f / ll;
-    const bool out32 = (p.flags & FA_OUT_FP32) != 0;
+    if (lane == 0) red[warp] = ll;
+    __syncthreads();
+    ll = 0.f;
 #pragma unroll
-    for (int k = 0; k < D / 32; ++k) {
-        const int d = lane + 32 * k;
-        float acc = 0.f;
-        if (!empty)
-            for (int s = 0; s < S; ++s) acc = fmaf(part[(size_t)s * (D + 2) + d], w[s], acc);
-        const float v = acc * inv;
-        if (out32)
-            static_cast<float*>(p.o)[row * D + d] = v;
-        else
-            static_cast<__nv_bfloat16*>(p.o)[row * D + d] = __float2bfloat16_rn(v);
+    for (int w = 0; w < D / 32; ++w) ll += red[w];
+    const bool empty = !(ll > 0.f);
+    // four independent partial sums keep four loads in flight
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (!empty) {
+        int s = 0;
+        for (; s + 4 <= S; s += 4) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) acc[u] = fmaf(part[(size_t)(s + u) * (D + 2) + tid], wts[s + u], acc[u]);
+        }
+        for (; s < S; ++s) acc[0] = fmaf(part[(size_t)s * (D + 2) + tid], wts[s], acc[0]);
     }
-    if (lane == 0) p.lse[row] = empty ? -CUDART_INF_F : (mm + log2f(ll)) * kLn2D;
+    const float v = empty ? 0.f : ((acc[0] + acc[1]) + (acc[2] + acc[3])) / ll;
+    if (p.flags & FA_OUT_FP32)
+        static_cast<float*>(p.o)[row * D + tid] = v;
+    else
+        static_cast<__nv_bfloat16*>(p.o)[row * D + tid] = __float2bfloat16_rn(v);
+    if (tid == 0) p.lse[row] = empty ? -CUDART_INF_F : (mm + log2f(ll)) * kLn2D;
 }
 
 template <int D, int SCORE>
@@ -463,7 +473,7 @@ cudaError_t launch_decode_d(const DecodeParams& p, const CUtensorMap& tk, const 
     }
     if (e != cudaSuccess) return e;
     const long long rows = (long long)p.B * p.Hq * p.q_len;
-    decode_combine_kernel<D><<<(unsigned)((rows + 3) / 4), 128, 4u * p.splits * sizeof(float), s>>>(p);
+    decode_combine_kernel<D><<<(unsigned)rows, D, p.splits * sizeof(float), s>>>(p);
     return cudaGetLastError();
 }
 

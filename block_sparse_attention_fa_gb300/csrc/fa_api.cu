@@ -317,20 +317,15 @@ int32_t fa_decode_splits(const fa_fwd_args* a, const fa_block_mask* bm) {
     if (!a || !bm || a->B < 1 || a->Hkv < 1 || a->Hq < 1 || bm->nkv < 1 || (bm->H != 1 && bm->H != a->Hq)) return 0;
     int rows, grouped, groups;
     decode_shape(a, bm, &rows, &grouped, &groups);
-    // One CTA per SM: the fewest waves times tiles per split, counting every
-    // kv tile of the row (the visited count lives on the device).
+    // Enough CTAs (one per SM) to keep about 80 % of the SMs streaming, each
+    // split at least 4 tiles long: per-CTA start-up (barriers, Q, the first
+    // copies in flight, the merge) costs about as much as a few tiles, and a
+    // CTA keeps three 128-row K/V tiles in flight, so that fewer CTAs than
+    // SMs already draw the full HBM bandwidth.
     const int sms = sm_count();
-    const int cap = std::min(bm->nkv, fa::decode_max_splits());
-    long long best = -1;
-    int best_s = 1;
-    for (int sp = 1; sp <= cap; ++sp) {
-        const long long waves = ((long long)groups * sp + sms - 1) / sms;
-        const long long cost = waves * ((bm->nkv + sp - 1) / sp);
-        if (best < 0 || cost < best) {
-            best = cost;
-            best_s = sp;
-        }
-    }
+    const int want = (int)((0.8 * sms + groups - 1) / groups);
+    const int cap = std::max(1, std::min(bm->nkv / 4, fa::decode_max_splits()));
+    const int best_s = std::max(1, std::min(want, cap));
     return best_s;
 }
 
@@ -355,6 +350,8 @@ fa_status fa_fwd_decode(const fa_fwd_args* a, const fa_block_mask* bm, const fa_
         return fail(FA_ERR_INVALID_ARG, "num_splits must be in [1, %d] or 0 (got %d)", fa::decode_max_splits(),
                     num_splits);
     if (groups > 65535) return fail(FA_ERR_UNSUPPORTED, "too many row groups (%d)", groups);
+    if ((long long)a->B * a->Hq * a->q_len > 2147483647LL)
+        return fail(FA_ERR_UNSUPPORTED, "too many query rows (%lld)", (long long)a->B * a->Hq * a->q_len);
     const size_t need = fa_decode_partials_bytes(a, num_splits);
     if (!partials || !aligned16(partials))
         return fail(FA_ERR_INVALID_ARG, "partials must be non-NULL and 16-byte aligned");

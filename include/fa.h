@@ -237,9 +237,10 @@ fa_status fa_fwd_decode(const fa_fwd_args *a, const fa_block_mask *bm, const fa_
  * count (0 if the arguments cannot be valid).                               */
 size_t fa_decode_partials_bytes(const fa_fwd_args *a, int32_t num_splits);
 
-/* The split count fa_fwd_decode uses for num_splits = 0: with one CTA per
- * SM of the current device, the count that minimises waves x tiles per split
- * over the row's nkv tiles (0 if the arguments cannot be valid).            */
+/* The split count fa_fwd_decode uses for num_splits = 0: enough splits that
+ * the row groups give about 0.8 CTAs per SM of the current device, but no
+ * fewer than 4 of the row's nkv tiles per split (0 if the arguments cannot
+ * be valid).                                                                */
 int32_t fa_decode_splits(const fa_fwd_args *a, const fa_block_mask *bm);
 
 /* Synchronise `stream`, then report and clear the device-side flags in
