@@ -530,6 +530,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="time only the split-KV decoding workloads and print their section")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -549,6 +551,12 @@ def main():
     peaks, peak_src = load_peaks()
     from block_sparse_attention_fa_gb300 import fa
     fa.load_library()
+
+    if args.decode_only:
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+        print(json.dumps({"decode": decode_section(device, flush, args.steps, args.warmup, peaks, peak_src)}),
+              flush=True)
+        return
 
     r = Runner(w, device)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)

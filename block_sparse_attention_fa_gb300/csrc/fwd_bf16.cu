@@ -11,9 +11,10 @@
 //
 // One persistent CTA per SM takes work units from a queue in the workspace.
 // A unit is a PAIR of adjacent 128-row query blocks (2p, 2p + 1) of one
-// (b, hq): the kv tiles of the two BlockMask rows are walked as one ascending
-// sequence (the union of the two rows' partial and full lists), each K/V
-// tile is loaded once and used by whichever of the two query tiles lists it.
+// (b, hq): the kv tiles of the two BlockMask rows are walked as one
+// descending sequence, diagonal first (the union of the two rows' partial and
+// full lists), each K/V tile is loaded once and used by whichever of the two
+// query tiles lists it.
 // Every kv tile is processed as two 64-column halves, each with its own S
 // buffer, so that the tensor pipe computes one half's S while the softmax
 // works on the other.  384 threads in five roles:
