@@ -27,7 +27,7 @@ _lock = threading.Lock()
 _handle = None
 
 MASK_KINDS = {"full": 0, "causal": 1, "sliding_window": 2, "document": 3, "prefix_lm": 4}
-SCORE_KINDS = {"none": 0, "softcap": 1, "alibi": 2, "rel_bias": 3}
+SCORE_KINDS = {"none": 0, "softcap": 1, "alibi": 2, "rel_bias": 3, "alibi_softcap": 4}
 
 
 class _Mask(ctypes.Structure):
@@ -118,7 +118,7 @@ def fwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, *, mask: str = "full", wind
     sc = _Score()
     sc.kind = SCORE_KINDS[score]
     sc.softcap = float(softcap)
-    if score == "alibi":
+    if score in ("alibi", "alibi_softcap"):
         sl = np.ascontiguousarray(slopes, dtype=np.float32)
         keep.append(sl)
         sc.slopes = sl.ctypes.data

@@ -24,6 +24,9 @@
  *               soft-capping formula S_ij = C tanh(q^T k / (C sqrt d)))
  *   ALiBi       s - slope[hq] * |i - j|   ("Implementation" script, the
  *               composite score_mod's bias term)
+ *   ALiBi then soft-cap   C * tanh((s - slope[hq] |i - j|) / C)
+ *               ("Implementation" script, composite_score_mod: bias added
+ *               first, the sum capped)
  *   rel. bias   s + table[hq][clamp(i - j, -R, R) + R]   (named in "The Core
  *               Design Principles", item 1, "position-dependent biases"; the
  *               table form is this library's reading)
@@ -45,7 +48,7 @@
 enum { OR_MASK_FULL = 0, OR_MASK_CAUSAL = 1, OR_MASK_SLIDING_WINDOW = 2,
        OR_MASK_DOCUMENT = 3, OR_MASK_PREFIX_LM = 4 };
 enum { OR_SCORE_NONE = 0, OR_SCORE_SOFTCAP = 1, OR_SCORE_ALIBI = 2,
-       OR_SCORE_REL_BIAS = 3 };
+       OR_SCORE_REL_BIAS = 3, OR_SCORE_ALIBI_SOFTCAP = 4 };
 
 typedef struct {
     int kind;
@@ -94,6 +97,12 @@ static double or_score_mod(const or_score *sc, double s, int h, int i, int j)
         return sc->softcap * tanh(s / sc->softcap);
     case OR_SCORE_ALIBI:
         return s - (double)sc->slopes[h] * fabs((double)(i - j));
+    case OR_SCORE_ALIBI_SOFTCAP: {
+        /* the "Implementation" script's composite_score_mod: the ALiBi bias
+           first, then the soft-cap of the biased score */
+        const double u = s - (double)sc->slopes[h] * fabs((double)(i - j));
+        return sc->softcap * tanh(u / sc->softcap);
+    }
     case OR_SCORE_REL_BIAS: {
         int r = i - j;
         if (r < -sc->rel_max) r = -sc->rel_max;

@@ -51,6 +51,51 @@ def test_softcap_limits():
     np.testing.assert_allclose(l_cap[..., 0], C * np.tanh(s00 / C), atol=1e-12)
 
 
+def test_alibi_then_softcap_closed_form():
+    """The composite score_mod of the guide's 'Implementation' script: bias
+    first, then the cap.  q = 0 makes every raw score 0, so the causal row
+    i = 2 sees u_j = -slope (2 - j); with slope = C ln 2 and C = 1 the capped
+    scores are C tanh(-ln 4), C tanh(-ln 2), 0 = -15/17, -3/5, 0
+    (tanh(ln a) = (a^2 - 1) / (a^2 + 1)).  Capping first and adding the bias
+    after would give -2 ln 2, -ln 2, 0 instead."""
+    C = 1.0
+    q = np.zeros((1, 1, 3, 1), np.float32)
+    k = np.ones((1, 1, 3, 1), np.float32)
+    v = np.array([1.0, 2.0, 4.0], np.float32).reshape(1, 1, 3, 1)
+    slopes = np.array([C * math.log(2.0)], np.float32)
+    o, lse = oracle.fwd(q, k, v, mask="causal", score="alibi_softcap", slopes=slopes, softcap=C)
+    sl = float(slopes[0]) / C                       # the float32 slope, in units of C
+    w = [math.exp(C * math.tanh(-2.0 * sl)), math.exp(C * math.tanh(-sl)), 1.0]
+    assert math.tanh(-2.0 * math.log(2.0)) == pytest.approx(-15.0 / 17.0, abs=1e-15)
+    assert math.tanh(-math.log(2.0)) == pytest.approx(-3.0 / 5.0, abs=1e-15)
+    assert o[0, 0, 2, 0] == pytest.approx((w[0] * 1 + w[1] * 2 + w[2] * 4) / sum(w), abs=1e-7)
+    assert lse[0, 0, 2] == pytest.approx(math.log(sum(w)), abs=1e-7)
+    assert o[0, 0, 2, 0] == pytest.approx((math.exp(-15 / 17) + 2 * math.exp(-0.6) + 4) /
+                                          (math.exp(-15 / 17) + math.exp(-0.6) + 1), abs=1e-6)
+    cap_first = [0.25, 0.5, 1.0]
+    assert abs(o[0, 0, 2, 0] - (0.25 + 1.0 + 4.0) / sum(cap_first)) > 0.1
+
+
+def test_alibi_then_softcap_reductions():
+    """Zero slopes give the plain soft-cap; a cap of 1e30 gives plain ALiBi."""
+    q, k, v = (_rand((1, 3, 50, 16), s, 2.0) for s in (11, 12, 13))
+    slopes = np.array([0.1, 0.45, 0.8], np.float32)
+    o_c, l_c = oracle.fwd(q, k, v, mask="sliding_window", window=20, score="alibi_softcap",
+                          slopes=np.zeros(3, np.float32), softcap=3.0)
+    o_s, l_s = oracle.fwd(q, k, v, mask="sliding_window", window=20, score="softcap", softcap=3.0)
+    np.testing.assert_allclose(o_c, o_s, atol=1e-13)
+    np.testing.assert_allclose(l_c, l_s, atol=1e-13)
+    o_c, l_c = oracle.fwd(q, k, v, mask="causal", score="alibi_softcap", slopes=slopes, softcap=1e30)
+    o_a, l_a = oracle.fwd(q, k, v, mask="causal", score="alibi", slopes=slopes)
+    np.testing.assert_allclose(o_c, o_a, atol=1e-12)
+    np.testing.assert_allclose(l_c, l_a, atol=1e-12)
+
+
+def test_composite_facts_of_the_page():
+    f = GOLDEN["composite_score_mod"]
+    assert f["order"] == ["alibi_bias", "softcap"] and f["softcap_C"] == GOLDEN["softcap_C"]["value"]
+
+
 def test_alibi_closed_form_and_sign():
     # q = 0 makes every raw score 0, so the weights are exp(-slope |i - j|).  With
     # slope = ln 2 and the causal row i = 2: 2^-2, 2^-1, 1 -> 1/7, 2/7, 4/7.
