@@ -44,7 +44,8 @@ from block_sparse_attention_fa_gb300 import synth  # noqa: E402
 METRIC = "fwd TFLOP/s on visited blocks & % of GB300 bf16 tensor peak; windows/s grouped"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 HEADLINE = "grouped_bf16"
-SECONDARY = ["document_bf16", "causal_softcap_bf16", "window_alibi_gqa_bf16", "grouped_fp32"]
+SECONDARY = ["document_bf16", "causal_softcap_bf16", "window_alibi_gqa_bf16", "window_alibi_softcap_bf16",
+             "grouped_fp32"]
 
 
 def load_peaks():
@@ -167,9 +168,9 @@ class Runner:
         self.q, self.k, self.v = (torch.from_numpy(x).to(device).to(dt) for x in (q, k, v))
         self.seg_d = torch.from_numpy(self.seg).to(device) if self.seg is not None else None
         self.score_kw = {"score": w.score}
-        if w.score == "softcap":
+        if w.score in ("softcap", "alibi_softcap"):
             self.score_kw["softcap"] = w.softcap
-        elif w.score == "alibi":
+        if w.score in ("alibi", "alibi_softcap"):
             self.score_kw["alibi_slopes"] = torch.from_numpy(w.slopes()).to(device)
         self.out = torch.empty_like(self.q)
         self.lse = torch.empty((w.B, w.Hq, w.T), dtype=torch.float32, device=device)

@@ -143,6 +143,10 @@ template <int SCORE>
 __device__ __forceinline__ float score_mod(const DecodeParams& p, float s, int hq, int i, int j) {
     if (SCORE == FA_SCORE_SOFTCAP) return p.score.softcap * tanhf(s / p.score.softcap);
     if (SCORE == FA_SCORE_ALIBI) return s - __ldg(p.score.slopes + hq) * fabsf(static_cast<float>(i - j));
+    if (SCORE == FA_SCORE_ALIBI_SOFTCAP) {
+        const float u = s - __ldg(p.score.slopes + hq) * fabsf(static_cast<float>(i - j));
+        return p.score.softcap * tanhf(u / p.score.softcap);
+    }
     if (SCORE == FA_SCORE_REL_BIAS) {
         const int R = p.score.rel_max;
         const int rr = min(max(i - j, -R), R);
@@ -469,6 +473,7 @@ cudaError_t launch_decode_d(const DecodeParams& p, const CUtensorMap& tk, const 
         case FA_SCORE_SOFTCAP: e = launch_split<D, FA_SCORE_SOFTCAP>(p, tk, tv, s); break;
         case FA_SCORE_ALIBI: e = launch_split<D, FA_SCORE_ALIBI>(p, tk, tv, s); break;
         case FA_SCORE_REL_BIAS: e = launch_split<D, FA_SCORE_REL_BIAS>(p, tk, tv, s); break;
+        case FA_SCORE_ALIBI_SOFTCAP: e = launch_split<D, FA_SCORE_ALIBI_SOFTCAP>(p, tk, tv, s); break;
         default: e = launch_split<D, FA_SCORE_NONE>(p, tk, tv, s); break;
     }
     if (e != cudaSuccess) return e;

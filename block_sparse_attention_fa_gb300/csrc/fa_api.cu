@@ -184,6 +184,11 @@ fa_status check_score(const fa_score_desc* sc, fa_score_desc* out) {
         case FA_SCORE_REL_BIAS:
             if (!sc->rel_bias || sc->rel_max < 0) return fail(FA_ERR_INVALID_ARG, "relative bias needs rel_bias and rel_max >= 0");
             break;
+        case FA_SCORE_ALIBI_SOFTCAP:
+            if (!sc->alibi_slopes) return fail(FA_ERR_INVALID_ARG, "ALiBi then soft-cap needs alibi_slopes");
+            if (!(sc->softcap > 0.f) || !std::isfinite(sc->softcap))
+                return fail(FA_ERR_INVALID_ARG, "softcap must be finite and > 0");
+            break;
         default: return fail(FA_ERR_INVALID_ARG, "unknown score kind %d", sc->kind);
     }
     *out = *sc;

@@ -658,10 +658,12 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const bool doc = p.mask.kind == FA_MASK_DOCUMENT;
         float cap_in = 0.f, cap_out = 0.f, s_lim = 0.f;
         float tq0 = 0.f, tq1 = 0.f, tq2 = 0.f, tq3 = 0.f, tq4 = 0.f;
-        if (SCORE == FA_SCORE_SOFTCAP) {
+        if (SCORE == FA_SCORE_SOFTCAP || SCORE == FA_SCORE_ALIBI_SOFTCAP) {
             // C log2(e) tanh(a s) = s Q(s^2), Q_k = C log2(e) a c_k a^(2k),
-            // valid while |a s| <= kTanhRange, i.e. |s| <= s_lim.
-            cap_in = p.scale / p.score.softcap;
+            // valid while |a s| <= kTanhRange, i.e. |s| <= s_lim.  s is the
+            // raw q.k for the soft-cap alone (a = scale / C) and the scaled,
+            // ALiBi-biased score for the composite (a = 1 / C).
+            cap_in = (SCORE == FA_SCORE_SOFTCAP ? p.scale : 1.f) / p.score.softcap;
             cap_out = p.score.softcap * kLog2e;
             const float a2 = cap_in * cap_in;
             const float base = cap_out * cap_in;
@@ -707,7 +709,11 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             // this thread's segment id in the first partial tile
             const int kp = c.rs.next_part();
             c.seg_next = (doc && kp >= 0 && kp * kBlock + r < p.kv_len) ? __ldg(seg_row + kp * kBlock + r) : INT_MAX;
-            c.slope_l2 = SCORE == FA_SCORE_ALIBI ? __ldg(p.score.slopes + c.pu.hq) * kLog2e : 0.f;
+            // the slope in the units the score has when the bias is added:
+            // base 2 for ALiBi alone, natural (before the cap) for the composite
+            c.slope_l2 = SCORE == FA_SCORE_ALIBI           ? __ldg(p.score.slopes + c.pu.hq) * kLog2e
+                         : SCORE == FA_SCORE_ALIBI_SOFTCAP ? __ldg(p.score.slopes + c.pu.hq)
+                                                           : 0.f;
             return true;
         };
         Cur cur;
@@ -781,9 +787,32 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     // into the exponent's FMA; otherwise x is the modified score
                     // in base-2 units.
                     float sc = 1.f;
-                    if (SCORE == FA_SCORE_NONE) {
-                        sc = sl2;
-                    } else if (SCORE == FA_SCORE_SOFTCAP) {
+                    if (SCORE == FA_SCORE_NONE) sc = sl2;
+                    if (SCORE == FA_SCORE_ALIBI || SCORE == FA_SCORE_ALIBI_SOFTCAP) {
+                        // bias -slope |i - j| (in base 2 for ALiBi alone; in
+                        // natural units, before the cap, for the composite); when
+                        // every (row, column) pair of the warp's rows and the
+                        // half's columns lies on one side of the diagonal it is
+                        // affine in the column: two packed FMAs per pair.
+                        const float sa = SCORE == FA_SCORE_ALIBI ? sl2 : p.scale;
+                        const float di = static_cast<float>(i - ch);
+                        const int wrow0 = qb * kBlock + wq * 32 - ch;     // i - ch of lane 0
+                        if (wrow0 - 63 >= 0 || wrow0 + 31 <= 0) {
+                            const float sgn = wrow0 >= 0 ? 1.f : -1.f;   // sign of i - j
+                            const float k0 = -sgn * slope_l2 * di, ks = sgn * slope_l2;
+#pragma unroll
+                            for (int e = 0; e < 64; e += 2) {
+                                float b0, b1;
+                                ffma2(b0, b1, ks, ks, static_cast<float>(e), static_cast<float>(e + 1), k0, k0);
+                                ffma2(x[e], x[e + 1], x[e], x[e + 1], sa, sa, b0, b1);
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 64; ++e)
+                                x[e] = fmaf(-slope_l2, fabsf(di - static_cast<float>(e)), x[e] * sa);
+                        }
+                    }
+                    if (SCORE == FA_SCORE_SOFTCAP || SCORE == FA_SCORE_ALIBI_SOFTCAP) {
                         // The polynomial holds while |s| <= s_lim.  One pass of
                         // |x| maxima decides, for the warp's 32 rows at once,
                         // between it and the exact form (rare for soft-cap
@@ -810,28 +839,8 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
                             for (int e = 0; e < 64; ++e) x[e] = softcap_exact(x[e] * cap_in, cap_out);
                         }
-                    } else if (SCORE == FA_SCORE_ALIBI) {
-                        // bias -slope |i - j|; when every (row, column) pair of
-                        // the warp's rows and the half's columns lies on one side
-                        // of the diagonal it is affine in the column: two packed
-                        // FMAs per pair.
-                        const float di = static_cast<float>(i - ch);
-                        const int wrow0 = qb * kBlock + wq * 32 - ch;     // i - ch of lane 0
-                        if (wrow0 - 63 >= 0 || wrow0 + 31 <= 0) {
-                            const float sgn = wrow0 >= 0 ? 1.f : -1.f;   // sign of i - j
-                            const float k0 = -sgn * slope_l2 * di, ks = sgn * slope_l2;
-#pragma unroll
-                            for (int e = 0; e < 64; e += 2) {
-                                float b0, b1;
-                                ffma2(b0, b1, ks, ks, static_cast<float>(e), static_cast<float>(e + 1), k0, k0);
-                                ffma2(x[e], x[e + 1], x[e], x[e + 1], sl2, sl2, b0, b1);
-                            }
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 64; ++e)
-                                x[e] = fmaf(-slope_l2, fabsf(di - static_cast<float>(e)), x[e] * sl2);
-                        }
-                    } else {
+                    }
+                    if (SCORE == FA_SCORE_REL_BIAS) {
 #pragma unroll
                         for (int e = 0; e < 64; ++e) {
                             const int rr = min(max(i - ch - e, -p.score.rel_max), p.score.rel_max);
@@ -1055,6 +1064,7 @@ cudaError_t launch_d(const FwdParams& p, const CUtensorMap& tq, const CUtensorMa
         case FA_SCORE_SOFTCAP: return launch_one<D, FA_SCORE_SOFTCAP>(p, tq, tk, tv, s);
         case FA_SCORE_ALIBI: return launch_one<D, FA_SCORE_ALIBI>(p, tq, tk, tv, s);
         case FA_SCORE_REL_BIAS: return launch_one<D, FA_SCORE_REL_BIAS>(p, tq, tk, tv, s);
+        case FA_SCORE_ALIBI_SOFTCAP: return launch_one<D, FA_SCORE_ALIBI_SOFTCAP>(p, tq, tk, tv, s);
         default: return launch_one<D, FA_SCORE_NONE>(p, tq, tk, tv, s);
     }
 }

@@ -74,7 +74,7 @@ __global__ void __launch_bounds__(kThreads32) fwd_fp32_kernel(const FwdParams p)
         doc ? p.mask.seg + (size_t)(p.mask.seg_batch == 1 ? 0 : b) * p.mask.seg_len : nullptr;
     const int my_seg = (doc && row_ok) ? seg_row[i] : 0;
     float slope = 0.f;
-    if (SCORE == FA_SCORE_ALIBI) slope = p.score.slopes[hq];
+    if (SCORE == FA_SCORE_ALIBI || SCORE == FA_SCORE_ALIBI_SOFTCAP) slope = p.score.slopes[hq];
     const float* rb = SCORE == FA_SCORE_REL_BIAS
                           ? p.score.rel_bias + (size_t)hq * (2 * p.score.rel_max + 1)
                           : nullptr;
@@ -132,6 +132,8 @@ __global__ void __launch_bounds__(kThreads32) fwd_fp32_kernel(const FwdParams p)
                 } else if (SCORE == FA_SCORE_REL_BIAS) {
                     const int r = min(max(i - col, -p.score.rel_max), p.score.rel_max);
                     x += rb[r + p.score.rel_max];
+                } else if (SCORE == FA_SCORE_ALIBI_SOFTCAP) {
+                    x = p.score.softcap * tanhf((x - slope * fabsf((float)(i - col))) / p.score.softcap);
                 }
                 bool keep = col < p.kv_len;
                 if (partial) {
@@ -198,6 +200,9 @@ cudaError_t launch_d(const FwdParams& p, cudaStream_t s) {
             break;
         case FA_SCORE_REL_BIAS:
             fwd_fp32_kernel<D, FA_SCORE_REL_BIAS><<<(unsigned)grid, kThreads32, 0, s>>>(p);
+            break;
+        case FA_SCORE_ALIBI_SOFTCAP:
+            fwd_fp32_kernel<D, FA_SCORE_ALIBI_SOFTCAP><<<(unsigned)grid, kThreads32, 0, s>>>(p);
             break;
         default:
             fwd_fp32_kernel<D, FA_SCORE_NONE><<<(unsigned)grid, kThreads32, 0, s>>>(p);

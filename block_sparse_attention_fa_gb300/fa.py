@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libfa_gb300.so")
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE_CHECK = range(6)
 BF16, FP32 = 0, 1
 MASK_KINDS = {"full": 0, "causal": 1, "sliding_window": 2, "document": 3, "prefix_lm": 4}
-SCORE_KINDS = {"none": 0, "softcap": 1, "alibi": 2, "rel_bias": 3}
+SCORE_KINDS = {"none": 0, "softcap": 1, "alibi": 2, "rel_bias": 3, "alibi_softcap": 4}
 OUT_FP32 = 1
 DEBUG_DROP_FIRST_LOAD = 1
 BLOCK = 128

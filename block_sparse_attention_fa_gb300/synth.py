@@ -89,6 +89,12 @@ def alibi_slopes(H: int) -> np.ndarray:
     return np.exp2(-8.0 * (h + 1.0) / H).astype(np.float32)
 
 
+def composite_slopes(H: int) -> np.ndarray:
+    """Slopes ``linspace(0.1, 0.8, H)``, as the guide's composite ALiBi +
+    soft-cap example draws them."""
+    return np.linspace(0.1, 0.8, H, dtype=np.float64).astype(np.float32)
+
+
 @dataclasses.dataclass
 class Workload:
     """A seeded synthetic attention problem (shapes, mask and score_mod)."""
@@ -131,7 +137,11 @@ class Workload:
         return document_segments(self.seed + 1000, self.B, self.T, self.doc_lo, self.doc_hi)
 
     def slopes(self) -> Optional[np.ndarray]:
-        return alibi_slopes(self.Hq) if self.score == "alibi" else None
+        if self.score == "alibi":
+            return alibi_slopes(self.Hq)
+        if self.score == "alibi_softcap":
+            return composite_slopes(self.Hq)
+        return None
 
     def rel_bias(self) -> Optional[np.ndarray]:
         """fp32 [Hq, 2R+1] relative-position bias table (seeded)."""
@@ -178,6 +188,9 @@ WORKLOADS = {
     "causal_softcap_bf16": Workload(
         name="causal_softcap_bf16", dtype="bf16", B=8, Hq=16, Hkv=16, T=4096, D=128,
         mask="causal", score="softcap", softcap=50.0, input_scale=2.0, seed=4),
+    "window_alibi_softcap_bf16": Workload(
+        name="window_alibi_softcap_bf16", dtype="bf16", B=2, Hq=8, Hkv=8, T=4096, D=64,
+        mask="sliding_window", window=512, score="alibi_softcap", softcap=50.0, seed=8),
     "window_alibi_gqa_bf16": Workload(
         name="window_alibi_gqa_bf16", dtype="bf16", B=1, Hq=32, Hkv=8, T=32768, D=128,
         mask="sliding_window", window=1024, score="alibi", seed=5),

@@ -68,7 +68,10 @@ typedef enum fa_score_kind {
     FA_SCORE_NONE = 0,           /* s                                               */
     FA_SCORE_SOFTCAP = 1,        /* softcap * tanh(s / softcap)                     */
     FA_SCORE_ALIBI = 2,          /* s - alibi_slopes[hq] * |i - j|                  */
-    FA_SCORE_REL_BIAS = 3        /* s + rel_bias[hq][clamp(i - j, -R, R) + R]       */
+    FA_SCORE_REL_BIAS = 3,       /* s + rel_bias[hq][clamp(i - j, -R, R) + R]       */
+    FA_SCORE_ALIBI_SOFTCAP = 4   /* softcap * tanh((s - alibi_slopes[hq] * |i - j|) / softcap):
+                                    the guide's composite_score_mod ("Implementation"
+                                    script), bias first, then the cap            */
 } fa_score_kind;
 
 /* A mask_mod and its parameters.
@@ -114,8 +117,8 @@ typedef struct fa_block_mask {
 } fa_block_mask;
 
 /* A score_mod and its parameters.
- *   softcap       SOFTCAP: C > 0.
- *   alibi_slopes  ALIBI: device fp32 [Hq], indexed by query head.
+ *   softcap       SOFTCAP, ALIBI_SOFTCAP: C > 0.
+ *   alibi_slopes  ALIBI, ALIBI_SOFTCAP: device fp32 [Hq], indexed by query head.
  *   rel_bias      REL_BIAS: device fp32 [Hq][2 * rel_max + 1].              */
 typedef struct fa_score_desc {
     int32_t kind;

@@ -27,11 +27,11 @@ def to_device(w, q, k, v):
 def score_kwargs_gpu(w):
     import torch
     kw = {"score": w.score}
-    if w.score == "softcap":
+    if w.score in ("softcap", "alibi_softcap"):
         kw["softcap"] = w.softcap
-    elif w.score == "alibi":
+    if w.score in ("alibi", "alibi_softcap"):
         kw["alibi_slopes"] = torch.from_numpy(w.slopes()).cuda()
-    elif w.score == "rel_bias":
+    if w.score == "rel_bias":
         kw["rel_bias"] = torch.from_numpy(w.rel_bias()).cuda()
         kw["rel_max"] = w.rel_max
     return kw
@@ -39,11 +39,11 @@ def score_kwargs_gpu(w):
 
 def score_kwargs_oracle(w):
     kw = {"score": w.score}
-    if w.score == "softcap":
+    if w.score in ("softcap", "alibi_softcap"):
         kw["softcap"] = w.softcap
-    elif w.score == "alibi":
+    if w.score in ("alibi", "alibi_softcap"):
         kw["slopes"] = w.slopes()
-    elif w.score == "rel_bias":
+    if w.score == "rel_bias":
         kw["rel_bias"] = w.rel_bias()
         kw["rel_max"] = w.rel_max
     return kw

@@ -50,7 +50,8 @@ def _check(w, **kw):
 
 
 MASKS = [("full", {}), ("causal", {}), ("sliding_window", {"window": 40}), ("prefix_lm", {"prefix_len": 300})]
-SCORES = [("none", {}), ("softcap", {"softcap": 5.0}), ("alibi", {}), ("rel_bias", {"rel_max": 40})]
+SCORES = [("none", {}), ("softcap", {"softcap": 5.0}), ("alibi", {}), ("rel_bias", {"rel_max": 40}),
+          ("alibi_softcap", {"softcap": 4.0})]
 
 
 @pytest.mark.parametrize("D", [64, 128])
@@ -59,7 +60,7 @@ SCORES = [("none", {}), ("softcap", {"softcap": 5.0}), ("alibi", {}), ("rel_bias
 def test_masks_and_scores(D, mask, mkw, score, skw):
     """kv_len 1000 leaves a ragged tail tile; splits 1, 3 and the library's
     choice rotate over the cases."""
-    splits = {"none": 1, "softcap": 3, "alibi": 0, "rel_bias": 5}[score]
+    splits = {"none": 1, "softcap": 3, "alibi": 0, "rel_bias": 5, "alibi_softcap": 2}[score]
     _check(_case(mask, score, D=D, **mkw, **skw), num_splits=splits)
 
 

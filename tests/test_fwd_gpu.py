@@ -37,7 +37,8 @@ def _check_full(w, out_fp32=False, max_abs=None):
 
 MASKS = [("full", {}), ("causal", {}), ("sliding_window", {"window": 150}), ("prefix_lm", {"prefix_len": 170}),
          ("document", {"doc_lo": 20, "doc_hi": 180})]
-SCORES = [("none", {}), ("softcap", {"softcap": 5.0}), ("alibi", {}), ("rel_bias", {"rel_max": 40})]
+SCORES = [("none", {}), ("softcap", {"softcap": 5.0}), ("alibi", {}), ("rel_bias", {"rel_max": 40}),
+          ("alibi_softcap", {"softcap": 4.0})]
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
