@@ -83,6 +83,29 @@ def document_segments(seed: int, B: int, T: int, lo: int = 256, hi: int = 2048) 
     return seg
 
 
+def tree_table(seed: int, B: int, context: int, n_tree: int) -> np.ndarray:
+    """Attend tables of speculative-decoding candidate trees (tree attention).
+
+    Per batch row, a tree of ``n_tree`` draft tokens: node 0 is the root and
+    node k > 0 hangs under a parent drawn uniformly from [0, k).  The queries
+    are the tree nodes (q_len = n_tree), the keys the ``context`` tokens
+    followed by the tree nodes (kv_len = context + n_tree).  Query k sees every
+    context key and the tree keys of its ancestors and itself.  Returns bool
+    [B, n_tree, context + n_tree].
+    """
+    rng = np.random.default_rng(seed)
+    t = np.zeros((B, n_tree, context + n_tree), dtype=bool)
+    t[:, :, :context] = True
+    for b in range(B):
+        parent = [-1] + [int(rng.integers(0, k)) for k in range(1, n_tree)]
+        for k in range(n_tree):
+            a = k
+            while a >= 0:
+                t[b, k, context + a] = True
+                a = parent[a]
+    return t
+
+
 def alibi_slopes(H: int) -> np.ndarray:
     """Geometric ALiBi slopes ``2^(-8 (h+1) / H)`` for query heads h = 0..H-1."""
     h = np.arange(H, dtype=np.float64)

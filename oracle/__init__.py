@@ -26,13 +26,15 @@ _LIB = os.path.join(_LIBDIR, "liboracle.so")
 _lock = threading.Lock()
 _handle = None
 
-MASK_KINDS = {"full": 0, "causal": 1, "sliding_window": 2, "document": 3, "prefix_lm": 4}
+MASK_KINDS = {"full": 0, "causal": 1, "sliding_window": 2, "document": 3, "prefix_lm": 4, "table": 5}
 SCORE_KINDS = {"none": 0, "softcap": 1, "alibi": 2, "rel_bias": 3, "alibi_softcap": 4}
 
 
 class _Mask(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int), ("window", ctypes.c_int), ("prefix_len", ctypes.c_int),
-                ("seg", ctypes.c_void_p), ("seg_batch", ctypes.c_int), ("seg_len", ctypes.c_int)]
+                ("seg", ctypes.c_void_p), ("seg_batch", ctypes.c_int), ("seg_len", ctypes.c_int),
+                ("table", ctypes.c_void_p), ("table_batch", ctypes.c_int), ("table_q", ctypes.c_int),
+                ("table_kv", ctypes.c_int)]
 
 
 class _Score(ctypes.Structure):
@@ -78,7 +80,8 @@ def default_threads() -> int:
     return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
 
 
-def _mask_struct(mask: str, window: int, prefix_len: int, seg: Optional[np.ndarray], keep: list):
+def _mask_struct(mask: str, window: int, prefix_len: int, seg: Optional[np.ndarray], keep: list,
+                 table: Optional[np.ndarray] = None, q_len: int = 0, kv_len: int = 0):
     m = _Mask()
     m.kind = MASK_KINDS[mask]
     m.window = int(window)
@@ -91,6 +94,15 @@ def _mask_struct(mask: str, window: int, prefix_len: int, seg: Optional[np.ndarr
         m.seg = s.ctypes.data
         m.seg_batch = s.shape[0]
         m.seg_len = s.shape[1]
+    if mask == "table":
+        t = np.ascontiguousarray(table, dtype=bool).astype(np.uint8)
+        if t.ndim == 2:
+            t = t[None]
+        if t.shape[1:] != (q_len, kv_len):
+            raise ValueError(f"table must be [batch, {q_len}, {kv_len}], got {t.shape}")
+        keep.append(t)
+        m.table = t.ctypes.data
+        m.table_batch, m.table_q, m.table_kv = t.shape
     return m
 
 
@@ -98,8 +110,11 @@ def fwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, *, mask: str = "full", wind
         prefix_len: int = 0, seg: Optional[np.ndarray] = None, score: str = "none",
         softcap: float = 0.0, slopes: Optional[np.ndarray] = None,
         rel_bias: Optional[np.ndarray] = None, rel_max: int = 0, scale: Optional[float] = None,
-        rows: Optional[np.ndarray] = None, threads: Optional[int] = None):
+        rows: Optional[np.ndarray] = None, threads: Optional[int] = None, table: Optional[np.ndarray] = None):
     """Attention output and logsumexp in float64.
+
+    mask "table": ``table`` is a bool array [batch (1 or B), Tq, Tkv] (or
+    [Tq, Tkv]); query i of batch b attends to key j where it is true.
 
     q: [B, Hq, Tq, D], k / v: [B, Hkv, Tkv, D] (any float dtype; upcast).
     rows: optional flat row indices ``(b * Hq + h) * Tq + i``; when given the
@@ -114,7 +129,7 @@ def fwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, *, mask: str = "full", wind
     if scale is None:
         scale = 1.0 / np.sqrt(D)
     keep: list = []
-    m = _mask_struct(mask, window, prefix_len, seg, keep)
+    m = _mask_struct(mask, window, prefix_len, seg, keep, table, Tq, Tkv)
     sc = _Score()
     sc.kind = SCORE_KINDS[score]
     sc.softcap = float(softcap)
@@ -146,10 +161,10 @@ def fwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, *, mask: str = "full", wind
 
 def block_mask(*, mask: str, B: int, H: int, q_len: int, kv_len: int, window: int = 0,
                prefix_len: int = 0, seg: Optional[np.ndarray] = None, block: int = 128,
-               threads: Optional[int] = None) -> dict:
+               threads: Optional[int] = None, table: Optional[np.ndarray] = None) -> dict:
     """Brute-force BlockMask (every in-range pair of every tile evaluated)."""
     keep: list = []
-    m = _mask_struct(mask, window, prefix_len, seg, keep)
+    m = _mask_struct(mask, window, prefix_len, seg, keep, table, q_len, kv_len)
     nq = (q_len + block - 1) // block
     nkv = (kv_len + block - 1) // block
     out = {

@@ -35,6 +35,9 @@
  *               sliding-window mask is causal and (q_idx - kv_idx) <= 512)
  *   document    seg[i] == seg[j]          ("Production Engineering", item 1)
  *   prefix-LM   j < P or i >= j           ("Production Engineering", item 2)
+ *   table       table[b][i][j] != 0       ("Production Engineering", item 3:
+ *               tree attention's parent-child relation as a direct index
+ *               lookup in mask_mod)
  *
  * The brute-force tile scan (oracle_block_mask) evaluates the same predicate
  * on every in-range pair of every 128 x 128 tile ("Systems Mechanics", item 1:
@@ -46,7 +49,7 @@
 #include <string.h>
 
 enum { OR_MASK_FULL = 0, OR_MASK_CAUSAL = 1, OR_MASK_SLIDING_WINDOW = 2,
-       OR_MASK_DOCUMENT = 3, OR_MASK_PREFIX_LM = 4 };
+       OR_MASK_DOCUMENT = 3, OR_MASK_PREFIX_LM = 4, OR_MASK_TABLE = 5 };
 enum { OR_SCORE_NONE = 0, OR_SCORE_SOFTCAP = 1, OR_SCORE_ALIBI = 2,
        OR_SCORE_REL_BIAS = 3, OR_SCORE_ALIBI_SOFTCAP = 4 };
 
@@ -57,6 +60,10 @@ typedef struct {
     const int32_t *seg;     /* document: [seg_batch, seg_len]           */
     int seg_batch;
     int seg_len;
+    const uint8_t *table;   /* table: [table_batch, table_q, table_kv], 1 = attend */
+    int table_batch;
+    int table_q;
+    int table_kv;
 } or_mask;
 
 typedef struct {
@@ -83,6 +90,12 @@ static int or_mask_mod(const or_mask *m, int b, int i, int j)
     }
     case OR_MASK_PREFIX_LM:
         return j < m->prefix_len || i >= j;
+    case OR_MASK_TABLE: {
+        /* a mask_mod that is a direct index lookup (tree attention's
+           ancestor table) */
+        const uint8_t *t = m->table + (size_t)(m->table_batch == 1 ? 0 : b) * m->table_q * m->table_kv;
+        return t[(size_t)i * m->table_kv + j] != 0;
+    }
     }
     return 0;
 }

@@ -96,6 +96,61 @@ def test_composite_facts_of_the_page():
     assert f["order"] == ["alibi_bias", "softcap"] and f["softcap_C"] == GOLDEN["softcap_C"]["value"]
 
 
+def test_table_mask_equal_to_causal_is_causal():
+    """A lookup table holding the causal predicate gives the causal result."""
+    q, k, v = (_rand((2, 2, 37, 8), s) for s in (21, 22, 23))
+    table = np.tril(np.ones((37, 37), bool))
+    o_t, l_t = oracle.fwd(q, k, v, mask="table", table=table, score="alibi", slopes=np.array([0.3, 0.7], np.float32))
+    o_c, l_c = oracle.fwd(q, k, v, mask="causal", score="alibi", slopes=np.array([0.3, 0.7], np.float32))
+    np.testing.assert_array_equal(o_t, o_c)
+    np.testing.assert_array_equal(l_t, l_c)
+
+
+def test_table_mask_tree_closed_form():
+    """Tree attention with q = 0 (all scores equal): each tree query averages
+    V over the context and its ancestors-or-self.  Tree parents 0 <- 1 <- 3,
+    0 <- 2; one context key."""
+    table = np.zeros((1, 4, 5), bool)
+    table[0, :, 0] = True                           # the context key
+    for node, anc in enumerate([[0], [0, 1], [0, 2], [0, 1, 3]]):
+        for a in anc:
+            table[0, node, 1 + a] = True
+    q = np.zeros((1, 1, 4, 1), np.float32)
+    k = np.ones((1, 1, 5, 1), np.float32)
+    v = np.array([1.0, 2.0, 4.0, 8.0, 16.0], np.float32).reshape(1, 1, 5, 1)
+    o, lse = oracle.fwd(q, k, v, mask="table", table=table)
+    np.testing.assert_allclose(o[0, 0, :, 0], [(1 + 2) / 2, (1 + 2 + 4) / 3, (1 + 2 + 8) / 3, (1 + 2 + 4 + 16) / 4],
+                               atol=1e-14)
+    np.testing.assert_allclose(lse[0, 0], np.log([2, 3, 3, 4]), atol=1e-14)
+
+
+def test_table_mask_per_batch_and_tree_generator():
+    """Each batch row reads its own table; the generated trees give every
+    query its context, itself and its root, and only ancestors otherwise."""
+    t = synth.tree_table(5, 2, 6, 9)
+    assert t.shape == (2, 9, 15)
+    assert t[:, :, :6].all() and all(t[b, k, 6 + k] and t[b, k, 6] for b in range(2) for k in range(9))
+    assert not np.triu(t[:, :, 6:], 1).any()        # no node sees a later node
+    q, k, v = (_rand((2, 1, 9, 4), s) for s in (31, 32, 33))
+    k, v = _rand((2, 1, 15, 4), 34), _rand((2, 1, 15, 4), 35)
+    o, _ = oracle.fwd(q, k, v, mask="table", table=t)
+    for b in range(2):
+        ob, _ = oracle.fwd(q[b:b + 1], k[b:b + 1], v[b:b + 1], mask="table", table=t[b])
+        np.testing.assert_array_equal(o[b], ob[0])
+
+
+def test_table_block_mask_matches_the_closed_form_kind():
+    """The brute-force BlockMask of a table holding the sliding-window
+    predicate equals that of the sliding-window kind, bit for bit."""
+    T, W = 700, 150
+    i, j = np.meshgrid(np.arange(T), np.arange(T), indexing="ij")
+    table = (i >= j) & (i - j <= W)
+    a = oracle.block_mask(mask="table", B=1, H=1, q_len=T, kv_len=T, table=table)
+    b = oracle.block_mask(mask="sliding_window", B=1, H=1, q_len=T, kv_len=T, window=W)
+    for key in a:
+        np.testing.assert_array_equal(a[key], b[key])
+
+
 def test_alibi_closed_form_and_sign():
     # q = 0 makes every raw score 0, so the weights are exp(-slope |i - j|).  With
     # slope = ln 2 and the causal row i = 2: 2^-2, 2^-1, 1 -> 1/7, 2/7, 4/7.
