@@ -362,7 +362,10 @@ def decode_section(device, flush, steps, warmup, peaks, peak_src):
     out = {}
     for name, w in synth.DECODE_WORKLOADS.items():
         q, k, v = (torch.from_numpy(x).to(device).to(torch.bfloat16) for x in w.qkv())
-        bm = fa.block_mask(w.mask, 1, 1, w.Tq, w.T, window=w.window, prefix_len=w.prefix_len)
+        table = w.table()
+        tab = torch.from_numpy(synth.pack_table(table)).to(device) if table is not None else None
+        bm = fa.block_mask(w.mask, tab.shape[0] if tab is not None else 1, 1, w.Tq, w.T, window=w.window,
+                           prefix_len=w.prefix_len, table=tab)
         splits = fa.decode_splits(q, k, bm)
         parts = fa.decode_partials(q, splits)
         o = torch.empty_like(q)

@@ -21,6 +21,8 @@
 //                            [seg[c0], seg[c1]], every id in between present;
 //                            some pair <=> the ranges overlap; all pairs <=>
 //                            all four ids are equal
+//   table    bit j of row i: no closed form; the tile's in-range bits are
+//            read (4 words per row) and OR-ed / AND-ed
 // (r0..r1, c0..c1 = the tile's in-range rows and columns).  A tile is full
 // only when it is also complete (128 x 128 pairs in range).
 //
@@ -63,6 +65,28 @@ __device__ __forceinline__ TileClass classify(const MaskParams& m, const int32_t
     }
 }
 
+// A lookup-table mask: whether any / every in-range pair of the tile has its
+// bit set.  c0 is a multiple of 128, so the tile's columns are words
+// c0 / 32 .. c0 / 32 + 3 of each row; bits past c1 are ignored.
+__device__ __forceinline__ TileClass classify_table(const MaskParams& m, const uint32_t* tab, int r0, int r1,
+                                                    int c0, int c1) {
+    bool any = false, all = true;
+    const int ncols = c1 - c0 + 1;
+    for (int r = r0; r <= r1; ++r) {
+        const uint32_t* w = tab + (size_t)r * m.table_words + (c0 >> 5);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int nb = ncols - 32 * k;
+            if (nb <= 0) break;
+            const uint32_t valid = nb >= 32 ? 0xffffffffu : ((1u << nb) - 1u);
+            const uint32_t bits = __ldg(w + k) & valid;
+            any |= bits != 0u;
+            all &= bits == valid;
+        }
+    }
+    return {any, all};
+}
+
 __global__ void __launch_bounds__(kBuildThreads) block_mask_kernel(const BuildParams p) {
     const int qb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -71,6 +95,9 @@ __global__ void __launch_bounds__(kBuildThreads) block_mask_kernel(const BuildPa
     const bool doc = p.mask.kind == FA_MASK_DOCUMENT;
     const int32_t* seg_row =
         doc ? p.mask.seg + (size_t)(p.mask.seg_batch == 1 ? 0 : b) * p.mask.seg_len : nullptr;
+    const bool table = p.mask.kind == FA_MASK_TABLE;
+    const uint32_t* tab =
+        table ? p.mask.table + (size_t)(p.mask.table_batch == 1 ? 0 : b) * p.q_len * p.mask.table_words : nullptr;
 
     // Document masks need sorted ids: each segment row is checked once, by the
     // CTAs of head 0 (and batch 0 when the row is shared), pairs (r, r + 1).
@@ -99,7 +126,8 @@ __global__ void __launch_bounds__(kBuildThreads) block_mask_kernel(const BuildPa
         if (kb < p.nkv) {
             const int c0 = kb * kBlock;
             const int c1 = min(c0 + kBlock - 1, p.kv_len - 1);
-            const TileClass t = classify(p.mask, seg_row, r0, r1, c0, c1);
+            const TileClass t = table ? classify_table(p.mask, tab, r0, r1, c0, c1)
+                                      : classify(p.mask, seg_row, r0, r1, c0, c1);
             const bool complete = q_complete && (c1 - c0) == kBlock - 1;
             full = t.any && t.all && complete;
             part = t.any && !full;

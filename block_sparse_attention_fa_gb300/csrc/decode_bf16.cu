@@ -128,12 +128,17 @@ __device__ __forceinline__ RowId row_id(const DecodeParams& p, int g, int r) {
 
 // mask_mod of a built-in predicate (only evaluated on partial tiles), with
 // the sequence bound.
-__device__ __forceinline__ bool visible(const DecodeParams& p, int i, int j) {
+__device__ __forceinline__ bool visible(const DecodeParams& p, int b, int i, int j) {
     if (j >= p.kv_len) return false;
     switch (p.mask.kind) {
         case FA_MASK_CAUSAL: return i >= j;
         case FA_MASK_SLIDING_WINDOW: return i >= j && i - j <= p.mask.window;
         case FA_MASK_PREFIX_LM: return j < p.mask.prefix_len || i >= j;
+        case FA_MASK_TABLE: {
+            const uint32_t* row =
+                p.mask.table + ((size_t)(p.mask.table_batch == 1 ? 0 : b) * p.q_len + i) * p.mask.table_words;
+            return (__ldg(row + (j >> 5)) >> (j & 31)) & 1u;
+        }
         default: return true;
     }
 }
@@ -295,7 +300,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                 float v = s[nt][c];
                 if (SCORE != FA_SCORE_NONE) v = score_mod<SCORE>(p, v * sc, rid[h].hq, rid[h].i, j);
                 v *= sl2;
-                if (partial && !visible(p, rid[h].i, j)) v = -CUDART_INF_F;
+                if (partial && !visible(p, rid[h].b, rid[h].i, j)) v = -CUDART_INF_F;
                 s[nt][c] = v;
                 mx[h] = fmaxf(mx[h], v);
             }

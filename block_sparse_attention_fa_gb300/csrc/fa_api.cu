@@ -61,6 +61,13 @@ fa_status check_mask_desc(const fa_mask_desc& m, int B, int q_len, int kv_len) {
             if (q_len != kv_len)
                 return fail(FA_ERR_UNSUPPORTED, "document mask needs q_len == kv_len (got %d, %d)", q_len, kv_len);
             return FA_OK;
+        case FA_MASK_TABLE:
+            if (!m.table) return fail(FA_ERR_INVALID_ARG, "table mask needs a table");
+            if (reinterpret_cast<uintptr_t>(m.table) & 3u)
+                return fail(FA_ERR_INVALID_ARG, "the mask table must be 4-byte aligned");
+            if (m.table_batch != 1 && m.table_batch != B)
+                return fail(FA_ERR_INVALID_ARG, "table_batch must be 1 or the mask's B=%d (got %d)", B, m.table_batch);
+            return FA_OK;
         default:
             return fail(FA_ERR_INVALID_ARG, "unknown mask kind %d", m.kind);
     }
@@ -95,6 +102,9 @@ fa::MaskParams mask_params(const fa_block_mask* bm) {
     m.seg_batch = bm->mask.seg_batch;
     m.seg = bm->mask.seg_ids;
     m.seg_len = bm->kv_len;
+    m.table = bm->mask.table;
+    m.table_batch = bm->mask.table_batch;
+    m.table_words = (bm->kv_len + 31) / 32;
     return m;
 }
 
@@ -163,6 +173,8 @@ fa_status check_fwd_args(const fa_fwd_args* a, const fa_block_mask* bm, void* wo
         return fail(FA_ERR_INVALID_ARG, "block mask H=%d must be 1 or %d", bm->H, a->Hq);
     if (bm->mask.kind == FA_MASK_DOCUMENT && bm->mask.seg_batch != 1 && bm->mask.seg_batch != a->B)
         return fail(FA_ERR_INVALID_ARG, "seg_batch must be 1 or B=%d", a->B);
+    if (bm->mask.kind == FA_MASK_TABLE && bm->mask.table_batch != 1 && bm->mask.table_batch != a->B)
+        return fail(FA_ERR_INVALID_ARG, "table_batch must be 1 or B=%d", a->B);
     return FA_OK;
 }
 

@@ -30,6 +30,9 @@ struct MaskParams {
     int seg_batch;
     const int32_t* seg;           // [seg_batch, seg_len]
     int seg_len;
+    const uint32_t* table;        // [table_batch, q_len, table_words] attend bits
+    int table_batch;
+    int table_words;              // ceil(kv_len / 32)
 };
 
 struct ScoreParams {

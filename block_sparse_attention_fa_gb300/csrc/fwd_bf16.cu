@@ -656,6 +656,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const uint32_t tO = tmem + 256u + D * t;
         const float sl2 = p.scale * kLog2e;
         const bool doc = p.mask.kind == FA_MASK_DOCUMENT;
+        const bool table = p.mask.kind == FA_MASK_TABLE;
         float cap_in = 0.f, cap_out = 0.f, s_lim = 0.f;
         float tq0 = 0.f, tq1 = 0.f, tq2 = 0.f, tq3 = 0.f, tq4 = 0.f;
         if (SCORE == FA_SCORE_SOFTCAP || SCORE == FA_SCORE_ALIBI_SOFTCAP) {
@@ -731,6 +732,11 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const bool active = !rs.empty();
             const int32_t* seg_row =
                 doc ? p.mask.seg + (size_t)(p.mask.seg_batch == 1 ? 0 : pu.b) * p.mask.seg_len : nullptr;
+            // a lookup-table mask: this row's attend bits (none for rows past q_len)
+            const uint32_t* tab_row =
+                (table && i < p.q_len)
+                    ? p.mask.table + ((size_t)(p.mask.table_batch == 1 ? 0 : pu.b) * p.q_len + i) * p.mask.table_words
+                    : nullptr;
             const float* rb = nullptr;
             if (SCORE == FA_SCORE_REL_BIAS) rb = p.score.rel_bias + (size_t)pu.hq * (2 * p.score.rel_max + 1);
 
@@ -772,6 +778,12 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 for (int h = 0; h < 2; ++h) {
                     const uint32_t tSh = tS + 64u * h;   // S_t,h; P_t,h in its first 32 columns
                     const int ch = c0 + 64 * h;          // kv index of the half's column 0
+                    // the row's table bits of this half, loaded before S is waited for
+                    uint32_t tw0 = 0u, tw1 = 0u;
+                    if (partial && tab_row) {
+                        tw0 = __ldg(tab_row + (ch >> 5));
+                        if (ch + 32 < p.kv_len) tw1 = __ldg(tab_row + (ch >> 5) + 1);
+                    }
                     if (!mbar_wait_warp(bar(B_S_FULL + 2 * t + h), n & 1, wc, S_S_FULL)) { ok = false; break; }
                     tc_fence_after();
                     float x[64];
@@ -854,7 +866,19 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     // [0, max(i, P - 1)], and for a document mask (ids
                     // non-decreasing) the columns whose id equals the row's
                     // (found above by counting in the tile's ids).
-                    if (partial) {
+                    if (partial && table) {
+                        // a lookup-table mask: bit e of the half's two words
+                        // (bits past kv_len ignored)
+                        const int nvalid = p.kv_len - ch;
+                        if (nvalid < 32) tw0 &= (1u << nvalid) - 1u;
+                        if (nvalid < 64) tw1 = nvalid <= 32 ? 0u : (tw1 & ((1u << (nvalid - 32)) - 1u));
+                        const float off = -CUDART_INF_F;
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            x[e] = (tw0 & (1u << e)) ? x[e] : off;
+                            x[32 + e] = (tw1 & (1u << e)) ? x[32 + e] : off;
+                        }
+                    } else if (partial) {
                         int lo = -ch, hi = p.kv_len - 1 - ch;
                         if (doc) {
                             lo = seg_lo - 64 * h;

@@ -73,6 +73,11 @@ __global__ void __launch_bounds__(kThreads32) fwd_fp32_kernel(const FwdParams p)
     const int32_t* seg_row =
         doc ? p.mask.seg + (size_t)(p.mask.seg_batch == 1 ? 0 : b) * p.mask.seg_len : nullptr;
     const int my_seg = (doc && row_ok) ? seg_row[i] : 0;
+    // a lookup-table mask: this row's attend bits
+    const uint32_t* tab_row =
+        (p.mask.kind == FA_MASK_TABLE && row_ok)
+            ? p.mask.table + ((size_t)(p.mask.table_batch == 1 ? 0 : b) * p.q_len + i) * p.mask.table_words
+            : nullptr;
     float slope = 0.f;
     if (SCORE == FA_SCORE_ALIBI || SCORE == FA_SCORE_ALIBI_SOFTCAP) slope = p.score.slopes[hq];
     const float* rb = SCORE == FA_SCORE_REL_BIAS
@@ -146,6 +151,9 @@ __global__ void __launch_bounds__(kThreads32) fwd_fp32_kernel(const FwdParams p)
                             keep = keep && (col < p.mask.prefix_len || i >= col);
                             break;
                         case FA_MASK_DOCUMENT: keep = keep && segs[jj] == my_seg; break;
+                        case FA_MASK_TABLE:
+                            keep = keep && tab_row && ((__ldg(tab_row + (col >> 5)) >> (col & 31)) & 1u);
+                            break;
                         default: break;
                     }
                 }

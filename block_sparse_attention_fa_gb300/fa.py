@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libfa_gb300.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE_CHECK = range(6)
 BF16, FP32 = 0, 1
-MASK_KINDS = {"full": 0, "causal": 1, "sliding_window": 2, "document": 3, "prefix_lm": 4}
+MASK_KINDS = {"full": 0, "causal": 1, "sliding_window": 2, "document": 3, "prefix_lm": 4, "table": 5}
 SCORE_KINDS = {"none": 0, "softcap": 1, "alibi": 2, "rel_bias": 3, "alibi_softcap": 4}
 OUT_FP32 = 1
 DEBUG_DROP_FIRST_LOAD = 1
@@ -37,7 +37,8 @@ class FAError(RuntimeError):
 
 class MaskDesc(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int32), ("window", ctypes.c_int32), ("prefix_len", ctypes.c_int32),
-                ("seg_batch", ctypes.c_int32), ("seg_ids", ctypes.c_void_p)]
+                ("seg_batch", ctypes.c_int32), ("seg_ids", ctypes.c_void_p), ("table", ctypes.c_void_p),
+                ("table_batch", ctypes.c_int32)]
 
 
 class BlockMaskStruct(ctypes.Structure):
@@ -158,7 +159,7 @@ def default_workspace(device, stream=None) -> Workspace:
 class BlockMask:
     """A BlockMask over 128 x 128 tiles (device int32 arrays + the mask_mod)."""
 
-    def __init__(self, B, H, q_len, kv_len, mask, window, prefix_len, seg_ids, device):
+    def __init__(self, B, H, q_len, kv_len, mask, window, prefix_len, seg_ids, device, table=None):
         lib = load_library()
         nq, nkv, ne = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int64()
         _check(lib.fa_block_mask_shape(B, H, q_len, kv_len, ctypes.byref(nq), ctypes.byref(nkv), ctypes.byref(ne)))
@@ -166,6 +167,7 @@ class BlockMask:
         self.nq, self.nkv = nq.value, nkv.value
         self.mask, self.window, self.prefix_len = mask, window, prefix_len
         self.seg_ids = seg_ids
+        self.table = table
         self.kv_num_blocks = torch.empty((B, H, self.nq), dtype=torch.int32, device=device)
         self.kv_indices = torch.empty((B, H, self.nq, self.nkv), dtype=torch.int32, device=device)
         self.full_kv_num_blocks = torch.empty((B, H, self.nq), dtype=torch.int32, device=device)
@@ -184,6 +186,9 @@ class BlockMask:
         if seg_ids is not None:
             s.mask.seg_batch = seg_ids.shape[0]
             s.mask.seg_ids = seg_ids.data_ptr()
+        if table is not None:
+            s.mask.table_batch = table.shape[0]
+            s.mask.table = table.data_ptr()
         self.struct = s
 
     def rebuild(self, stream=None, workspace: Optional["Workspace"] = None):
@@ -203,9 +208,20 @@ class BlockMask:
 
 
 def block_mask(mask: str, B: int, H: int, q_len: int, kv_len: int, *, window: int = 0, prefix_len: int = 0,
-               seg_ids: Optional[torch.Tensor] = None, device=None, stream=None,
-               workspace: Optional[Workspace] = None) -> BlockMask:
-    """Build a BlockMask (fa_block_mask_build) for a built-in mask_mod."""
+               seg_ids: Optional[torch.Tensor] = None, table: Optional[torch.Tensor] = None, device=None,
+               stream=None, workspace: Optional[Workspace] = None) -> BlockMask:
+    """Build a BlockMask (fa_block_mask_build) for a built-in mask_mod.
+
+    mask "table": ``table`` is the packed lookup table of the C ABI, a CUDA
+    int32 tensor [table_batch, q_len, ceil(kv_len / 32)] whose bit j % 32 of
+    word j // 32 in row i says whether query i attends to key j."""
+    if table is not None:
+        if table.dim() == 2:
+            table = table[None]
+        if table.dtype != torch.int32 or not table.is_cuda or tuple(table.shape[1:]) != (q_len, (kv_len + 31) // 32):
+            raise ValueError("table must be a CUDA int32 tensor [batch, q_len, ceil(kv_len / 32)]")
+        table = table.contiguous()
+        device = table.device
     if seg_ids is not None:
         if seg_ids.dim() == 1:
             seg_ids = seg_ids[None]
@@ -214,7 +230,7 @@ def block_mask(mask: str, B: int, H: int, q_len: int, kv_len: int, *, window: in
         seg_ids = seg_ids.contiguous()
         device = seg_ids.device
     device = torch.device(device or "cuda")
-    bm = BlockMask(B, H, q_len, kv_len, mask, window, prefix_len, seg_ids, device)
+    bm = BlockMask(B, H, q_len, kv_len, mask, window, prefix_len, seg_ids, device, table=table)
     ws = workspace or default_workspace(device, stream)
     _check(load_library().fa_block_mask_build(ctypes.byref(bm.struct), ws.ptr, _stream_ptr(stream)))
     return bm

@@ -106,6 +106,20 @@ def tree_table(seed: int, B: int, context: int, n_tree: int) -> np.ndarray:
     return t
 
 
+def pack_table(table: np.ndarray) -> np.ndarray:
+    """A bool attend table [batch, q_len, kv_len] in the C ABI's packed form:
+    int32 [batch, q_len, ceil(kv_len / 32)], bit j % 32 (least significant
+    first) of word j // 32."""
+    t = np.asarray(table, dtype=bool)
+    if t.ndim == 2:
+        t = t[None]
+    pad = (-t.shape[2]) % 32
+    t = np.concatenate([t, np.zeros(t.shape[:2] + (pad,), bool)], axis=2)
+    bits = t.reshape(t.shape[0], t.shape[1], -1, 32).astype(np.uint64)
+    words = (bits << np.arange(32, dtype=np.uint64)).sum(axis=3).astype(np.uint32)
+    return words.view(np.int32)
+
+
 def alibi_slopes(H: int) -> np.ndarray:
     """Geometric ALiBi slopes ``2^(-8 (h+1) / H)`` for query heads h = 0..H-1."""
     h = np.arange(H, dtype=np.float64)
@@ -142,6 +156,7 @@ class Workload:
     seed: int = 0
     groups: Optional[int] = None   # number of independent windows (grouped workloads)
     q_len: Optional[int] = None    # query rows when they differ from T (decoding shapes)
+    tree: int = 0                  # table mask: candidate trees of this many tokens after T - tree context keys
 
     @property
     def Tq(self) -> int:
@@ -158,6 +173,12 @@ class Workload:
         if self.group > 0:
             return group_segments(self.T, self.group)[None, :].copy()
         return document_segments(self.seed + 1000, self.B, self.T, self.doc_lo, self.doc_hi)
+
+    def table(self) -> Optional[np.ndarray]:
+        """bool [B, Tq, T] attend table for table masks (candidate trees)."""
+        if self.mask != "table":
+            return None
+        return tree_table(self.seed + 3000, self.B, self.T - self.tree, self.tree)
 
     def slopes(self) -> Optional[np.ndarray]:
         if self.score == "alibi":
@@ -196,6 +217,11 @@ DECODE_WORKLOADS = {
     "decode_spec4_bf16": Workload(
         name="decode_spec4_bf16", dtype="bf16", B=8, Hq=32, Hkv=8, T=32768, D=128,
         mask="full", seed=7, q_len=4),
+    # tree attention: a 4-token candidate tree per sequence after 32768
+    # context tokens, its tokens querying the context and their ancestors
+    "decode_tree_bf16": Workload(
+        name="decode_tree_bf16", dtype="bf16", B=8, Hq=32, Hkv=8, T=32768 + 4, D=128,
+        mask="table", seed=9, q_len=4, tree=4),
 }
 
 WORKLOADS = {

@@ -58,7 +58,8 @@ typedef enum fa_mask_kind {
     FA_MASK_CAUSAL = 1,          /* i >= j                                          */
     FA_MASK_SLIDING_WINDOW = 2,  /* i >= j and i - j <= window (inclusive edge)     */
     FA_MASK_DOCUMENT = 3,        /* seg[b][i] == seg[b][j] (document / group packing) */
-    FA_MASK_PREFIX_LM = 4        /* j < prefix_len or i >= j                        */
+    FA_MASK_PREFIX_LM = 4,       /* j < prefix_len or i >= j                        */
+    FA_MASK_TABLE = 5            /* bit j of row i of a lookup table (tree attention) */
 } fa_mask_kind;
 
 /* Built-in score_mods on the scaled score s = scale * q.k (FlexAttention
@@ -82,13 +83,23 @@ typedef enum fa_score_kind {
  *               checks the order on the device; a violation sets
  *               FA_ERR_DEVICE_CHECK in the workspace.  DOCUMENT requires
  *               q_len == kv_len (one id per token of the packed sequence).
- *   seg_batch   DOCUMENT: 1 (shared by every batch row) or the mask's B.   */
+ *   seg_batch   DOCUMENT: 1 (shared by every batch row) or the mask's B.
+ *   table       TABLE: a mask_mod given as a direct index lookup, as tree
+ *               attention expresses a candidate tree's parent-child relation
+ *               (FlexAttention Guide, "Production Engineering", item 3).
+ *               Device uint32 [table_batch][q_len][ceil(kv_len / 32)],
+ *               4-byte aligned: query i of batch b attends to key j when bit
+ *               (j % 32) (least significant first) of word [b][i][j / 32] is
+ *               set.  Bits past kv_len are ignored.
+ *   table_batch TABLE: 1 (shared by every batch row) or the mask's B.       */
 typedef struct fa_mask_desc {
     int32_t kind;
     int32_t window;
     int32_t prefix_len;
     int32_t seg_batch;
     const int32_t *seg_ids;
+    const uint32_t *table;
+    int32_t table_batch;
 } fa_mask_desc;
 
 /* A BlockMask over 128 x 128 tiles (FlexAttention Guide, "The Core Design

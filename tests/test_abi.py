@@ -56,7 +56,8 @@ def test_struct_layout_matches_header(fa, tmp_path):
 int main(void) {
   printf("fa_mask_desc %zu\nfa_block_mask %zu\nfa_score_desc %zu\nfa_fwd_args %zu\n",
          sizeof(fa_mask_desc), sizeof(fa_block_mask), sizeof(fa_score_desc), sizeof(fa_fwd_args));
-  F(fa_mask_desc, seg_ids) F(fa_block_mask, kv_num_blocks) F(fa_block_mask, full_kv_indices)
+  F(fa_mask_desc, seg_ids) F(fa_mask_desc, table) F(fa_mask_desc, table_batch)
+  F(fa_block_mask, kv_num_blocks) F(fa_block_mask, full_kv_indices)
   F(fa_block_mask, mask) F(fa_score_desc, alibi_slopes) F(fa_score_desc, rel_max)
   F(fa_fwd_args, scale) F(fa_fwd_args, q) F(fa_fwd_args, lse) F(fa_fwd_args, timeout_ms)
   F(fa_fwd_args, flags) F(fa_fwd_args, debug_flags)
@@ -128,6 +129,9 @@ def _args(fa, **kw):
     ({"mask_kind": 3, "mask_seg_ids": FAKE, "mask_seg_batch": 2}, "ERR_INVALID_ARG", b"seg_batch"),
     ({"mask_kind": 3, "mask_seg_ids": FAKE, "mask_seg_batch": 1, "kv_len": 200, "nkv": 2},
      "ERR_UNSUPPORTED", b"q_len == kv_len"),
+    ({"mask_kind": 5}, "ERR_INVALID_ARG", b"needs a table"),
+    ({"mask_kind": 5, "mask_table": FAKE + 2, "mask_table_batch": 1}, "ERR_INVALID_ARG", b"aligned"),
+    ({"mask_kind": 5, "mask_table": FAKE, "mask_table_batch": 2}, "ERR_INVALID_ARG", b"table_batch"),
 ])
 def test_block_mask_build_rejects(fa, kw, status, text):
     lib = fa.load_library()

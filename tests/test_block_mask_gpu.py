@@ -85,3 +85,34 @@ def test_builder_full_size_workloads(fa, name):
         assert got["full_kv_num_blocks"].sum() == 1764 and got["kv_num_blocks"].sum() == 504
     if name == "grouped_bf16":
         assert got["full_kv_num_blocks"].sum() == 0 and got["kv_num_blocks"].sum() == 1568
+
+
+def _tables():
+    """(name, bool table [batch, q_len, kv_len]): candidate trees behind a
+    context, the window predicate as a table, and random blocky tables with
+    empty, full and partial tiles (ragged edges included)."""
+    rng = np.random.default_rng(9)
+    out = [("tree", synth.tree_table(3, 2, 300, 40)), ("tree_long", synth.tree_table(4, 1, 1000, 129))]
+    i, j = np.meshgrid(np.arange(700), np.arange(700), indexing="ij")
+    out.append(("window", ((i >= j) & (i - j <= 150))[None]))
+    for q_len, kv_len in [(300, 333), (128, 256), (1, 129), (257, 31)]:
+        coarse = rng.random((2, (q_len + 63) // 64, (kv_len + 63) // 64))
+        t = np.repeat(np.repeat(coarse, 64, 1), 64, 2)[:, :q_len, :kv_len]
+        dense = rng.random((2, q_len, kv_len)) < 0.5
+        out.append((f"blocky {q_len}x{kv_len}", np.where(t < 0.3, False, np.where(t > 0.7, True, dense))))
+    return out
+
+
+@pytest.mark.parametrize("name,table", _tables(), ids=[n for n, _ in _tables()])
+@pytest.mark.parametrize("H", [1, 3])
+def test_builder_tables(fa, name, table, H):
+    """Lookup-table masks: each batch row's own table, bits read per tile."""
+    import torch
+    Bt, q_len, kv_len = table.shape
+    tab = torch.from_numpy(synth.pack_table(table)).cuda()
+    bm = fa.block_mask("table", Bt, H, q_len, kv_len, table=tab)
+    fa.default_workspace(torch.device("cuda")).check()
+    got = bm.numpy()
+    want = oracle.block_mask(mask="table", B=Bt, H=H, q_len=q_len, kv_len=kv_len, table=table)
+    for key in want:
+        np.testing.assert_array_equal(got[key], want[key], err_msg=f"{name} {key}")

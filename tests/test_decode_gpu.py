@@ -34,13 +34,19 @@ def _run(w, num_splits=0, per_head=False, out_fp32=False):
     from block_sparse_attention_fa_gb300 import fa
     q, k, v = w.qkv()
     qd, kd, vd = parity.to_device(w, q, k, v)
-    bm = fa.block_mask(w.mask, 1, w.Hq if per_head else 1, w.Tq, w.T, window=w.window,
-                       prefix_len=w.prefix_len)
+    table = w.table()
+    tab = torch.from_numpy(synth.pack_table(table)).cuda() if table is not None else None
+    bm = fa.block_mask(w.mask, tab.shape[0] if tab is not None else 1, w.Hq if per_head else 1, w.Tq, w.T,
+                       window=w.window, prefix_len=w.prefix_len, table=tab)
     o, lse = fa.fwd_decode(qd, kd, vd, bm, num_splits=num_splits, out_fp32=out_fp32,
                            **parity.score_kwargs_gpu(w))
     fa.default_workspace(qd.device).check()
     torch.cuda.synchronize()
-    o_ref, lse_ref = parity.run_oracle(w, q, k, v, None)
+    if table is not None:
+        import oracle
+        o_ref, lse_ref = oracle.fwd(q, k, v, mask="table", table=table, **parity.score_kwargs_oracle(w))
+    else:
+        o_ref, lse_ref = parity.run_oracle(w, q, k, v, None)
     return (o.double().cpu().numpy(), lse.double().cpu().numpy()), (o_ref, lse_ref)
 
 
@@ -139,3 +145,21 @@ def test_full_size_decode_workloads(name):
     """The bench's decoding shapes, split count chosen by the library, every
     row against the oracle (each row reads the whole 32768-key sequence)."""
     _check(synth.DECODE_WORKLOADS[name])
+
+
+@pytest.mark.parametrize("q_len,Hq,Hkv,splits", [(4, 8, 2, 0), (16, 4, 4, 3), (3, 16, 4, 7)])
+def test_tree_attention_tables(q_len, Hq, Hkv, splits):
+    """Speculative-decoding verification: the draft tree's tokens query the
+    context and their ancestors through a lookup-table mask."""
+    import torch
+    from block_sparse_attention_fa_gb300 import fa
+    table = synth.tree_table(41 + q_len, 2, 1500, q_len)
+    w = _case("table", "alibi", B=2, Hq=Hq, Hkv=Hkv, q_len=q_len, kv_len=1500 + q_len, D=128)
+    q, k, v = w.qkv()
+    qd, kd, vd = parity.to_device(w, q, k, v)
+    bm = fa.block_mask("table", 2, 1, q_len, w.T, table=torch.from_numpy(synth.pack_table(table)).cuda())
+    o, lse = fa.fwd_decode(qd, kd, vd, bm, num_splits=splits, **parity.score_kwargs_gpu(w))
+    fa.default_workspace(qd.device).check()
+    import oracle
+    o_ref, lse_ref = oracle.fwd(q, k, v, mask="table", table=table, **parity.score_kwargs_oracle(w))
+    parity.compare(o.double().cpu().numpy(), o_ref, lse.double().cpu().numpy(), lse_ref, "bf16", label="tree")

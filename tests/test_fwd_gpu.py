@@ -196,3 +196,34 @@ def test_repeated_launches_are_bitwise_identical(name):
     for o, lse in outs[1:]:
         assert torch.equal(o.view(torch.int16), outs[0][0].view(torch.int16))
         assert torch.equal(lse, outs[0][1])
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("case", ["tree", "square"])
+def test_table_masks(dtype, D, case):
+    """Lookup-table masks: candidate trees behind a 700-token context (tree
+    attention, q_len = tree size) and a random blocky square table; each batch
+    row reads its own table."""
+    import torch
+    from block_sparse_attention_fa_gb300 import fa
+    if case == "tree":
+        table = synth.tree_table(17, 2, 700, 150)
+    else:
+        rng = np.random.default_rng(5)
+        coarse = rng.random((2, 6, 6))
+        t = np.repeat(np.repeat(coarse, 64, 1), 64, 2)[:, :333, :333]
+        table = np.where(t < 0.3, False, np.where(t > 0.7, True, rng.random((2, 333, 333)) < 0.4))
+    Bt, q_len, kv_len = table.shape
+    w = _case(dtype, "table", "alibi_softcap", B=2, Hq=4, Hkv=2, T=kv_len, D=D, softcap=6.0)
+    _, k, v = w.qkv()
+    q = synth.standard_normal(99, (2, 4, q_len, D))
+    if dtype == "bf16":
+        q = synth.round_to_bf16(q)
+    qd, kd, vd = parity.to_device(w, q, k, v)
+    bm = fa.block_mask("table", Bt, 1, q_len, kv_len, table=torch.from_numpy(synth.pack_table(table)).cuda())
+    o, lse = fa.fwd(qd, kd, vd, bm, **parity.score_kwargs_gpu(w))
+    fa.default_workspace(qd.device).check()
+    import oracle
+    o_ref, lse_ref = oracle.fwd(q, k, v, mask="table", table=table, **parity.score_kwargs_oracle(w))
+    parity.compare(o.double().cpu().numpy(), o_ref, lse.double().cpu().numpy(), lse_ref, dtype, label=case)
