@@ -128,18 +128,13 @@ __device__ __forceinline__ RowId row_id(const DecodeParams& p, int g, int r) {
 
 // mask_mod of a built-in predicate (only evaluated on partial tiles), with
 // the sequence bound.
-__device__ __forceinline__ bool visible(const DecodeParams& p, int b, int i, int j) {
+__device__ __forceinline__ bool visible(const DecodeParams& p, int i, int j) {
     if (j >= p.kv_len) return false;
     switch (p.mask.kind) {
         case FA_MASK_CAUSAL: return i >= j;
         case FA_MASK_SLIDING_WINDOW: return i >= j && i - j <= p.mask.window;
         case FA_MASK_PREFIX_LM: return j < p.mask.prefix_len || i >= j;
-        case FA_MASK_TABLE: {
-            const uint32_t* row =
-                p.mask.table + ((size_t)(p.mask.table_batch == 1 ? 0 : b) * p.q_len + i) * p.mask.table_words;
-            return (__ldg(row + (j >> 5)) >> (j & 31)) & 1u;
-        }
-        default: return true;
+        default: return true;   // FULL; TABLE is read per tile by the caller
     }
 }
 
@@ -265,6 +260,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
 #pragma unroll
     for (int dt = 0; dt < D / 8; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
     const float sc = p.scale;
+    const bool table = p.mask.kind == FA_MASK_TABLE;
     const float sl2 = SCORE == FA_SCORE_NONE ? p.scale * kLog2eD : kLog2eD;   // to base 2
     bool ok = true;
 
@@ -275,6 +271,19 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         const int kb = partial ? __ldg(part_idx + e) : __ldg(full_idx + (e - np));
         const uint32_t kbase = sbase + st * L::kStage;
         const uint32_t vbase = kbase + (D / 64) * L::kBox;
+        // A lookup-table mask: the warp's 16 keys share one 32-bit word of
+        // each row; bit 8 nt + 2 tq + c of tbits[h] is key j of the loop below.
+        uint32_t tbits[2] = {0u, 0u};
+        const int j0 = kb * kBlock + 16 * warp;
+        if (table && partial && j0 < p.kv_len) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t* row = p.mask.table +
+                                      ((size_t)(p.mask.table_batch == 1 ? 0 : rid[h].b) * p.q_len + rid[h].i) *
+                                          p.mask.table_words;
+                tbits[h] = __ldg(row + (j0 >> 5)) >> (j0 & 31);
+            }
+        }
 
         // S (16 rows x this warp's 16 keys) = Q K^T
         float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -300,7 +309,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                 float v = s[nt][c];
                 if (SCORE != FA_SCORE_NONE) v = score_mod<SCORE>(p, v * sc, rid[h].hq, rid[h].i, j);
                 v *= sl2;
-                if (partial && !visible(p, rid[h].b, rid[h].i, j)) v = -CUDART_INF_F;
+                const bool vis = table ? (j < p.kv_len && ((tbits[h] >> (8 * nt + 2 * tq + (c & 1))) & 1u))
+                                       : visible(p, rid[h].i, j);
+                if (partial && !vis) v = -CUDART_INF_F;
                 s[nt][c] = v;
                 mx[h] = fmaxf(mx[h], v);
             }
