@@ -68,6 +68,12 @@ def _lib():
             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
             ctypes.c_double, ctypes.POINTER(_Mask), ctypes.POINTER(_Score),
             ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+        h.oracle_bwd.restype = ctypes.c_int
+        h.oracle_bwd.argtypes = [
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            ctypes.c_double, ctypes.POINTER(_Mask), ctypes.POINTER(_Score),
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
         h.oracle_block_mask.restype = ctypes.c_int
         h.oracle_block_mask.argtypes = [
             ctypes.POINTER(_Mask), ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -157,6 +163,47 @@ def fwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, *, mask: str = "full", wind
     if full:
         return o.reshape(B, Hq, Tq, D), lse.reshape(B, Hq, Tq)
     return o, lse
+
+
+def bwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, dout: np.ndarray, *, mask: str = "full", window: int = 0,
+        prefix_len: int = 0, seg: Optional[np.ndarray] = None, score: str = "none", softcap: float = 0.0,
+        slopes: Optional[np.ndarray] = None, rel_bias: Optional[np.ndarray] = None, rel_max: int = 0,
+        scale: Optional[float] = None, threads: Optional[int] = None, table: Optional[np.ndarray] = None):
+    """Gradients (dq, dk, dv) in float64 of sum(O * dout) for the forward's
+    arguments; dout has O's shape [B, Hq, Tq, D]."""
+    q = np.ascontiguousarray(q, dtype=np.float32)
+    k = np.ascontiguousarray(k, dtype=np.float32)
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    g = np.ascontiguousarray(dout, dtype=np.float32)
+    B, Hq, Tq, D = q.shape
+    Hkv, Tkv = k.shape[1], k.shape[2]
+    if g.shape != q.shape:
+        raise ValueError("dout must have q's shape")
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    keep: list = []
+    m = _mask_struct(mask, window, prefix_len, seg, keep, table, Tq, Tkv)
+    sc = _Score()
+    sc.kind = SCORE_KINDS[score]
+    sc.softcap = float(softcap)
+    if score in ("alibi", "alibi_softcap"):
+        sl = np.ascontiguousarray(slopes, dtype=np.float32)
+        keep.append(sl)
+        sc.slopes = sl.ctypes.data
+    if score == "rel_bias":
+        rb = np.ascontiguousarray(rel_bias, dtype=np.float32)
+        keep.append(rb)
+        sc.rel_bias = rb.ctypes.data
+        sc.rel_max = int(rel_max)
+    dq = np.empty((B, Hq, Tq, D), dtype=np.float64)
+    dk = np.empty((B, Hkv, Tkv, D), dtype=np.float64)
+    dv = np.empty((B, Hkv, Tkv, D), dtype=np.float64)
+    rc = _lib().oracle_bwd(q.ctypes.data, k.ctypes.data, v.ctypes.data, g.ctypes.data, B, Hq, Hkv, Tq, Tkv, D,
+                           float(scale), ctypes.byref(m), ctypes.byref(sc), dq.ctypes.data, dk.ctypes.data,
+                           dv.ctypes.data, threads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_bwd rejected its arguments")
+    return dq, dk, dv
 
 
 def block_mask(*, mask: str, B: int, H: int, q_len: int, kv_len: int, window: int = 0,

@@ -126,6 +126,23 @@ static double or_score_mod(const or_score *sc, double s, int h, int i, int j)
     return s;
 }
 
+/* d score_mod / d s at the scaled score s (the biases do not depend on s). */
+static double or_score_mod_ds(const or_score *sc, double s, int h, int i, int j)
+{
+    switch (sc->kind) {
+    case OR_SCORE_SOFTCAP: {
+        const double t = tanh(s / sc->softcap);
+        return 1.0 - t * t;
+    }
+    case OR_SCORE_ALIBI_SOFTCAP: {
+        const double u = s - (double)sc->slopes[h] * fabs((double)(i - j));
+        const double t = tanh(u / sc->softcap);
+        return 1.0 - t * t;
+    }
+    }
+    return 1.0;
+}
+
 /*
  * Attention rows.  q: [B, Hq, Tq, D], k, v: [B, Hkv, Tkv, D] (fp32 values,
  * exact copies of bf16 inputs where the inputs are bf16).  rows[r] is the
@@ -253,4 +270,108 @@ int oracle_block_mask(const or_mask *mask, int Bm, int Hm, int Tq, int Tkv, int 
         }
     }
     return 0;
+}
+
+
+/*
+ * Gradients of the forward with respect to q, k and v for an upstream dO
+ * (the backward pass the FlexAttention Guide's "Implementation" script takes
+ * through autograd): for every query row (b, hq, i), with P_j the row's
+ * softmax weights as in the forward,
+ *     dP_j    = dO_i . v_j
+ *     Delta_i = sum_j P_j dP_j
+ *     dS_j    = P_j (dP_j - Delta_i) * d score_mod / d s (s_j)
+ *     dq_i    = scale sum_j dS_j k_j
+ *     dk_j   += scale dS_j q_i,   dv_j += P_j dO_i
+ * (masked pairs have P_j = 0; a row that attends to nothing contributes
+ * nothing).  dq: [B, Hq, Tq, D], dk, dv: [B, Hkv, Tkv, D], all written.
+ * Each kv head (b, hk) is one task, so dk and dv need no reduction across
+ * threads.  Returns 0, or -1 on bad arguments.
+ */
+int oracle_bwd(const float *q, const float *k, const float *v, const float *dout,
+               int B, int Hq, int Hkv, int Tq, int Tkv, int D, double scale,
+               const or_mask *mask, const or_score *score,
+               double *dq, double *dk, double *dv, int nthreads)
+{
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Tq <= 0 || Tkv <= 0 || D <= 0)
+        return -1;
+    const int group = Hq / Hkv;
+    int bad = 0;
+
+#pragma omp parallel num_threads(nthreads > 0 ? nthreads : 1) reduction(| : bad)
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)Tkv);
+        double *sraw = (double *)malloc(sizeof(double) * (size_t)Tkv);
+        double *p = (double *)malloc(sizeof(double) * (size_t)Tkv);
+        double *dp = (double *)malloc(sizeof(double) * (size_t)Tkv);
+        if (!s || !sraw || !p || !dp) {
+            bad = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int task = 0; task < B * Hkv; ++task) {
+                const int b = task / Hkv, hk = task % Hkv;
+                const float *kb = k + ((size_t)b * Hkv + hk) * (size_t)Tkv * D;
+                const float *vb = v + ((size_t)b * Hkv + hk) * (size_t)Tkv * D;
+                double *dkb = dk + ((size_t)b * Hkv + hk) * (size_t)Tkv * D;
+                double *dvb = dv + ((size_t)b * Hkv + hk) * (size_t)Tkv * D;
+                for (size_t x = 0; x < (size_t)Tkv * D; ++x) dkb[x] = dvb[x] = 0.0;
+                for (int hq = hk * group; hq < (hk + 1) * group; ++hq) {
+                    for (int i = 0; i < Tq; ++i) {
+                        const size_t row = ((size_t)b * Hq + hq) * Tq + i;
+                        const float *qi = q + row * D;
+                        const float *gi = dout + row * D;
+                        double *dqi = dq + row * D;
+                        for (int d = 0; d < D; ++d) dqi[d] = 0.0;
+                        /* the forward's row: scores, mask, softmax weights */
+                        double M = -INFINITY;
+                        for (int j = 0; j < Tkv; ++j) {
+                            const float *kj = kb + (size_t)j * D;
+                            double dot = 0.0;
+                            for (int d = 0; d < D; ++d)
+                                dot += (double)qi[d] * (double)kj[d];
+                            sraw[j] = scale * dot;
+                            double sj = or_score_mod(score, sraw[j], hq, i, j);
+                            if (!or_mask_mod(mask, b, i, j))
+                                sj = -INFINITY;
+                            s[j] = sj;
+                            if (sj > M) M = sj;
+                        }
+                        if (M == -INFINITY) continue;
+                        double L = 0.0;
+                        for (int j = 0; j < Tkv; ++j) {
+                            p[j] = s[j] == -INFINITY ? 0.0 : exp(s[j] - M);
+                            L += p[j];
+                        }
+                        double delta = 0.0;
+                        for (int j = 0; j < Tkv; ++j) {
+                            p[j] /= L;
+                            const float *vj = vb + (size_t)j * D;
+                            double t = 0.0;
+                            for (int d = 0; d < D; ++d)
+                                t += (double)gi[d] * (double)vj[d];
+                            dp[j] = t;
+                            delta += p[j] * t;
+                        }
+                        for (int j = 0; j < Tkv; ++j) {
+                            if (p[j] == 0.0) continue;
+                            const double ds = p[j] * (dp[j] - delta) * or_score_mod_ds(score, sraw[j], hq, i, j);
+                            const float *kj = kb + (size_t)j * D;
+                            double *dkj = dkb + (size_t)j * D;
+                            double *dvj = dvb + (size_t)j * D;
+                            for (int d = 0; d < D; ++d) {
+                                dqi[d] += scale * ds * (double)kj[d];
+                                dkj[d] += scale * ds * (double)qi[d];
+                                dvj[d] += p[j] * (double)gi[d];
+                            }
+                        }
+                    }
+                }
+            }
+        }
+        free(s);
+        free(sraw);
+        free(p);
+        free(dp);
+    }
+    return bad ? -1 : 0;
 }

@@ -400,3 +400,83 @@ def test_block_mask_broadcast_and_tail():
     np.testing.assert_array_equal(bm["full_kv_num_blocks"][0, 0], [2, 2, 0])
     for h in range(3):
         np.testing.assert_array_equal(bm["kv_indices"][1, h], bm["kv_indices"][1, 0])
+
+
+# ------------------------------------------------------------------ backward
+
+def _quantized(shape, seed, scale=1.0):
+    """Values on a 2^-8 grid, so that adding +-2^-10 is exact in float32."""
+    return np.round(_rand(shape, seed, scale) * 256.0) / 256.0
+
+
+def _fd_grads(fwd_kw, q, k, v, g, eps=2.0 ** -10):
+    """Central differences of sum(O * g) through the oracle's forward."""
+    def loss(q_, k_, v_):
+        o, _ = oracle.fwd(q_, k_, v_, **fwd_kw)
+        return float((o * g).sum())
+    out = []
+    for which in range(3):
+        arrs = [q.copy(), k.copy(), v.copy()]
+        grad = np.zeros(arrs[which].shape)
+        for idx in np.ndindex(arrs[which].shape):
+            a = [x.copy() for x in arrs]
+            a[which][idx] += eps
+            up = loss(*a)
+            a[which][idx] -= 2 * eps
+            dn = loss(*a)
+            grad[idx] = (up - dn) / (2 * eps)
+        out.append(grad)
+    return out
+
+
+BWD_MASKS = [("full", {}), ("causal", {}), ("sliding_window", {"window": 2}),
+             ("table", {"table": np.array([[1, 0, 1, 0, 0, 1], [0, 0, 0, 0, 0, 0], [1, 1, 1, 1, 0, 0],
+                                           [0, 1, 0, 1, 1, 1]], bool)})]
+BWD_SCORES = [("none", {}), ("softcap", {"softcap": 1.5}), ("alibi", {"slopes": np.array([0.3, 0.9], np.float32)}),
+              ("rel_bias", {"rel_max": 2, "rel_bias": np.array([[0.5, -1.0, 0.25, 2.0, -0.5],
+                                                                [1.0, 0.0, -0.75, 0.5, 0.125]], np.float32)}),
+              ("alibi_softcap", {"softcap": 1.5, "slopes": np.array([0.3, 0.9], np.float32)})]
+
+
+@pytest.mark.parametrize("mask,mkw", BWD_MASKS, ids=[m for m, _ in BWD_MASKS])
+@pytest.mark.parametrize("score,skw", BWD_SCORES, ids=[s for s, _ in BWD_SCORES])
+def test_backward_matches_finite_differences(mask, mkw, score, skw):
+    """dq, dk, dv of sum(O * dO) against central differences of the forward,
+    GQA (2 query heads on 1 kv head), Tq != Tkv; the table leaves row 1 with
+    no key (its gradients are zero)."""
+    q = _quantized((1, 2, 4, 3), 41, 1.5)
+    k = _quantized((1, 1, 6, 3), 42, 1.5)
+    v = _quantized((1, 1, 6, 3), 43)
+    g = _rand((1, 2, 4, 3), 44)
+    kw = {"mask": mask, "score": score, **mkw, **skw}
+    dq, dk, dv = oracle.bwd(q, k, v, g, **kw)
+    fq, fk, fv = _fd_grads(kw, q, k, v, g)
+    np.testing.assert_allclose(dq, fq, atol=2e-6)
+    np.testing.assert_allclose(dk, fk, atol=2e-6)
+    np.testing.assert_allclose(dv, fv, atol=2e-6)
+
+
+def test_backward_invariants():
+    """Softmax rows sum to one: sum_j dv_j = sum_i dO_i over the rows that
+    attend; and with every key equal, S does not depend on q: dq = 0."""
+    q, k, v, g = (_rand((1, 2, 30, 8), s).astype(np.float32) for s in (51, 52, 53, 54))
+    _, dk, dv = oracle.bwd(q, k, v, g, mask="causal")
+    np.testing.assert_allclose(dv.sum(axis=2), g.astype(np.float64).sum(axis=2), atol=1e-12)
+    k_eq = np.repeat(k[:, :, :1], 30, axis=2)
+    dq, _, _ = oracle.bwd(q, k_eq, v, g, mask="full")
+    np.testing.assert_allclose(dq, 0.0, atol=1e-12)
+
+
+def test_backward_gqa_is_the_sum_over_the_group():
+    """dK, dV of a shared kv head equal the sums of the per-head gradients with
+    K and V repeated for every query head."""
+    q, g = _rand((1, 4, 20, 8), 61), _rand((1, 4, 20, 8), 62)
+    k, v = _rand((1, 2, 20, 8), 63), _rand((1, 2, 20, 8), 64)
+    dq, dk, dv = oracle.bwd(q, k, v, g, mask="sliding_window", window=5, score="alibi",
+                            slopes=np.array([0.1, 0.2, 0.3, 0.4], np.float32))
+    kr, vr = np.repeat(k, 2, axis=1), np.repeat(v, 2, axis=1)
+    dq2, dk2, dv2 = oracle.bwd(q, kr, vr, g, mask="sliding_window", window=5, score="alibi",
+                               slopes=np.array([0.1, 0.2, 0.3, 0.4], np.float32))
+    np.testing.assert_allclose(dq, dq2, atol=1e-13)
+    np.testing.assert_allclose(dk, dk2.reshape(1, 2, 2, 20, 8).sum(axis=2), atol=1e-12)
+    np.testing.assert_allclose(dv, dv2.reshape(1, 2, 2, 20, 8).sum(axis=2), atol=1e-12)
