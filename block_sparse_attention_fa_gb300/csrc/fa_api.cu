@@ -407,6 +407,70 @@ fa_status fa_fwd_decode(const fa_fwd_args* a, const fa_block_mask* bm, const fa_
     return ok();
 }
 
+fa_status fa_bwd(const fa_bwd_args* a, const fa_block_mask* bm, const fa_score_desc* sc, void* stream) {
+    if (!a) return fail(FA_ERR_INVALID_ARG, "bwd args are NULL");
+    if (a->B < 1 || a->Hq < 1 || a->Hkv < 1 || a->q_len < 1 || a->kv_len < 1)
+        return fail(FA_ERR_INVALID_ARG, "extents must be >= 1 (B=%d Hq=%d Hkv=%d q_len=%d kv_len=%d)", a->B,
+                    a->Hq, a->Hkv, a->q_len, a->kv_len);
+    if (a->Hq % a->Hkv != 0)
+        return fail(FA_ERR_INVALID_ARG, "Hq (%d) must be a multiple of Hkv (%d)", a->Hq, a->Hkv);
+    if (a->D != 64 && a->D != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d not supported (64 or 128)", a->D);
+    if (!a->q || !a->k || !a->v || !a->o || !a->dout || !a->lse || !a->dq || !a->dk || !a->dv || !a->delta)
+        return fail(FA_ERR_INVALID_ARG, "q, k, v, o, dout, lse, dq, dk, dv and delta must be non-NULL");
+    if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v) || !aligned16(a->o) || !aligned16(a->dout))
+        return fail(FA_ERR_INVALID_ARG, "q, k, v, o and dout must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(a->dq) | reinterpret_cast<uintptr_t>(a->dk) |
+         reinterpret_cast<uintptr_t>(a->dv)) & 7u)
+        return fail(FA_ERR_INVALID_ARG, "dq, dk and dv must be 8-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(a->lse) | reinterpret_cast<uintptr_t>(a->delta)) & 3u)
+        return fail(FA_ERR_INVALID_ARG, "lse and delta must be 4-byte aligned");
+    if (!(std::isfinite(a->scale))) return fail(FA_ERR_INVALID_ARG, "scale must be finite");
+    fa_status st = check_block_mask(bm);
+    if (st != FA_OK) return st;
+    if (bm->q_len != a->q_len || bm->kv_len != a->kv_len)
+        return fail(FA_ERR_INVALID_ARG, "block mask was built for (%d, %d), not (%d, %d)", bm->q_len, bm->kv_len,
+                    a->q_len, a->kv_len);
+    if (bm->B != 1 && bm->B != a->B) return fail(FA_ERR_INVALID_ARG, "block mask B=%d must be 1 or %d", bm->B, a->B);
+    if (bm->H != 1 && bm->H != a->Hq)
+        return fail(FA_ERR_INVALID_ARG, "block mask H=%d must be 1 or %d", bm->H, a->Hq);
+    if (bm->mask.kind == FA_MASK_DOCUMENT && bm->mask.seg_batch != 1 && bm->mask.seg_batch != a->B)
+        return fail(FA_ERR_INVALID_ARG, "seg_batch must be 1 or B=%d", a->B);
+    if (bm->mask.kind == FA_MASK_TABLE && bm->mask.table_batch != 1 && bm->mask.table_batch != a->B)
+        return fail(FA_ERR_INVALID_ARG, "table_batch must be 1 or B=%d", a->B);
+    if ((long long)a->B * a->Hq > 65535) return fail(FA_ERR_UNSUPPORTED, "B x Hq must be <= 65535");
+    if ((long long)a->B * a->Hq * a->q_len > 2147483647LL)
+        return fail(FA_ERR_UNSUPPORTED, "too many query rows");
+    fa_score_desc score;
+    if ((st = check_score(sc, &score)) != FA_OK) return st;
+
+    fa::BwdParams p{};
+    p.B = a->B;
+    p.Hq = a->Hq;
+    p.Hkv = a->Hkv;
+    p.q_len = a->q_len;
+    p.kv_len = a->kv_len;
+    p.D = a->D;
+    p.group = a->Hq / a->Hkv;
+    p.scale = a->scale > 0.f ? a->scale : 1.0f / std::sqrt((float)a->D);
+    p.bm = {bm->B, bm->H, bm->nq, bm->nkv, bm->kv_num_blocks, bm->kv_indices, bm->full_kv_num_blocks,
+            bm->full_kv_indices};
+    p.mask = mask_params(bm);
+    p.score = {score.kind, score.softcap, score.alibi_slopes, score.rel_bias, score.rel_max};
+    p.q = a->q;
+    p.k = a->k;
+    p.v = a->v;
+    p.o = a->o;
+    p.dout = a->dout;
+    p.lse = a->lse;
+    p.delta = a->delta;
+    p.dq = a->dq;
+    p.dk = a->dk;
+    p.dv = a->dv;
+    cudaError_t e = fa::launch_bwd_bf16(p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+    return ok();
+}
+
 fa_status fa_workspace_check(void* workspace, void* stream) {
     if (!workspace) return fail(FA_ERR_INVALID_ARG, "workspace is NULL");
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -81,6 +81,25 @@ struct DecodeParams {
     uint32_t flags;
 };
 
+// The backward (bwd_bf16.cu).
+struct BwdParams {
+    int B, Hq, Hkv, q_len, kv_len, D, group;
+    float scale;
+    BlockMaskView bm;
+    MaskParams mask;
+    ScoreParams score;
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* o;                // the forward's output (bf16)
+    const void* dout;             // upstream gradient of O (bf16)
+    const float* lse;             // the forward's logsumexp
+    float* delta;                 // scratch [B][Hq][q_len]: rowsum(dO * O)
+    float* dq;
+    float* dk;
+    float* dv;
+};
+
 struct BuildParams {
     int B, H, q_len, kv_len, nq, nkv;
     MaskParams mask;
@@ -101,6 +120,7 @@ cudaError_t launch_fwd_bf16(const FwdParams& p, const CUtensorMap& tq, const CUt
                             const CUtensorMap& tv, cudaStream_t s);
 cudaError_t launch_decode_bf16(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                                cudaStream_t s);
+cudaError_t launch_bwd_bf16(const BwdParams& p, cudaStream_t s);
 int decode_max_splits();
 int decode_max_rows();
 

@@ -25,7 +25,7 @@ DEBUG_DROP_FIRST_LOAD = 1
 BLOCK = 128
 
 SYMBOLS = ("fa_workspace_bytes", "fa_block_mask_shape", "fa_block_mask_build", "fa_fwd",
-           "fa_fwd_noalloc", "fa_fwd_decode", "fa_decode_partials_bytes", "fa_decode_splits",
+           "fa_fwd_noalloc", "fa_fwd_decode", "fa_decode_partials_bytes", "fa_decode_splits", "fa_bwd",
            "fa_workspace_check", "fa_last_error", "fa_version")
 
 
@@ -65,6 +65,14 @@ class FwdArgs(ctypes.Structure):
                 ("debug_flags", ctypes.c_uint32)]
 
 
+class BwdArgs(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32), ("q_len", ctypes.c_int32),
+                ("kv_len", ctypes.c_int32), ("D", ctypes.c_int32), ("scale", ctypes.c_float),
+                ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("o", ctypes.c_void_p),
+                ("dout", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("dq", ctypes.c_void_p),
+                ("dk", ctypes.c_void_p), ("dv", ctypes.c_void_p), ("delta", ctypes.c_void_p)]
+
+
 _lib = None
 
 
@@ -98,6 +106,9 @@ def load_library(path: str = LIB_PATH):
     h.fa_decode_partials_bytes.argtypes = [ctypes.POINTER(FwdArgs), ctypes.c_int32]
     h.fa_decode_splits.restype = ctypes.c_int32
     h.fa_decode_splits.argtypes = [ctypes.POINTER(FwdArgs), ctypes.POINTER(BlockMaskStruct)]
+    h.fa_bwd.restype = ctypes.c_int
+    h.fa_bwd.argtypes = [ctypes.POINTER(BwdArgs), ctypes.POINTER(BlockMaskStruct), ctypes.POINTER(ScoreDesc),
+                         ctypes.c_void_p]
     h.fa_workspace_check.restype = ctypes.c_int
     h.fa_workspace_check.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
     h.fa_last_error.restype = ctypes.c_char_p
@@ -381,6 +392,33 @@ def fwd_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, bm: BlockMask,
                              ctypes.c_void_p(partials.data_ptr()), partials.numel() * partials.element_size(),
                              ws.ptr, _stream_ptr(stream)))
     return out, lse
+
+
+def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse: torch.Tensor,
+        dout: torch.Tensor, bm: BlockMask, *, score: str = "none", softcap: float = 0.0,
+        alibi_slopes: Optional[torch.Tensor] = None, rel_bias: Optional[torch.Tensor] = None, rel_max: int = 0,
+        scale: Optional[float] = None, dq: Optional[torch.Tensor] = None, dk: Optional[torch.Tensor] = None,
+        dv: Optional[torch.Tensor] = None, delta: Optional[torch.Tensor] = None, stream=None):
+    """Backward of fwd (fa_bwd) for bf16 q, k, v, the forward's bf16 o and
+    its lse, and the upstream gradient dout; returns fp32 (dq, dk, dv)."""
+    for t in (q, k, v, o, dout):
+        if t.dtype != torch.bfloat16 or not (t.is_cuda and t.is_contiguous() and t.dim() == 4):
+            raise ValueError("q, k, v, o and dout must be contiguous CUDA bf16 tensors [B, H, T, D]")
+    B, Hq, Tq, D = q.shape
+    Hkv, Tkv = k.shape[1], k.shape[2]
+    f32 = dict(dtype=torch.float32, device=q.device)
+    dq = torch.empty((B, Hq, Tq, D), **f32) if dq is None else dq
+    dk = torch.empty((B, Hkv, Tkv, D), **f32) if dk is None else dk
+    dv = torch.empty((B, Hkv, Tkv, D), **f32) if dv is None else dv
+    delta = torch.empty((B, Hq, Tq), **f32) if delta is None else delta
+    a = BwdArgs()
+    a.B, a.Hq, a.Hkv, a.q_len, a.kv_len, a.D = B, Hq, Hkv, Tq, Tkv, D
+    a.scale = 0.0 if scale is None else float(scale)
+    a.q, a.k, a.v, a.o, a.dout = q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr()
+    a.lse, a.dq, a.dk, a.dv, a.delta = lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), delta.data_ptr()
+    sc = _score_desc(score, softcap, alibi_slopes, rel_bias, rel_max)
+    _check(load_library().fa_bwd(ctypes.byref(a), ctypes.byref(bm.struct), ctypes.byref(sc), _stream_ptr(stream)))
+    return dq, dk, dv
 
 
 def version() -> str:

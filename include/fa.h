@@ -257,6 +257,42 @@ size_t fa_decode_partials_bytes(const fa_fwd_args *a, int32_t num_splits);
  * be valid).                                                                */
 int32_t fa_decode_splits(const fa_fwd_args *a, const fa_block_mask *bm);
 
+/* Backward of fa_fwd: the gradients of a loss with respect to q, k and v,
+ * given its gradient dO with respect to O (the backward the FlexAttention
+ * Guide's "Implementation" script takes through autograd), for the same
+ * BlockMask, score_mod and scale as the forward call:
+ *     P = exp(S' - lse) (S' the forward's masked, score_mod'ed scores),
+ *     dP = dO V^T, Delta_i = sum_d dO_id O_id, dS = P o (dP - Delta) o
+ *     d score_mod / d s, dV = P^T dO, dK = scale dS^T Q, dQ = scale dS K.
+ * Only the tiles the BlockMask lists are visited, and the mask is evaluated
+ * on partial tiles only.
+ *   q, k, v   as for fa_fwd, bf16.
+ *   o, lse    the forward's bf16 O (flags 0) and lse of the same call.
+ *   dout      device bf16 [B][Hq][q_len][D].
+ *   dq        device fp32 [B][Hq][q_len][D]; dk, dv device fp32
+ *             [B][Hkv][kv_len][D] (summed over the query heads of each kv
+ *             head).  All three are written in full.
+ *   delta     device fp32 scratch [B][Hq][q_len].
+ * bf16 tensors 16-byte aligned, dq, dk, dv 8-byte, lse and delta 4-byte.
+ * Three kernel launches, asynchronous on `stream`; no device-side waits, so
+ * no workspace.                                                             */
+typedef struct fa_bwd_args {
+    int32_t B, Hq, Hkv, q_len, kv_len, D;
+    float scale;
+    const void *q;
+    const void *k;
+    const void *v;
+    const void *o;
+    const void *dout;
+    const float *lse;
+    float *dq;
+    float *dk;
+    float *dv;
+    float *delta;
+} fa_bwd_args;
+
+fa_status fa_bwd(const fa_bwd_args *a, const fa_block_mask *bm, const fa_score_desc *sc, void *stream);
+
 /* Synchronise `stream`, then report and clear the device-side flags in
  * `workspace`: FA_OK, FA_ERR_TIMEOUT or FA_ERR_DEVICE_CHECK (details in
  * fa_last_error()), or FA_ERR_CUDA if the stream itself reports an error.  */

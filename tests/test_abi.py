@@ -31,7 +31,7 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted([
-        "fa_block_mask_build", "fa_block_mask_shape", "fa_decode_partials_bytes", "fa_decode_splits", "fa_fwd",
+        "fa_block_mask_build", "fa_block_mask_shape", "fa_bwd", "fa_decode_partials_bytes", "fa_decode_splits", "fa_fwd",
         "fa_fwd_decode", "fa_fwd_noalloc", "fa_last_error", "fa_version", "fa_workspace_bytes",
         "fa_workspace_check"])
 
@@ -54,8 +54,10 @@ def test_struct_layout_matches_header(fa, tmp_path):
 #include "fa.h"
 #define F(T, m) printf(#T "." #m " %zu\n", offsetof(T, m));
 int main(void) {
-  printf("fa_mask_desc %zu\nfa_block_mask %zu\nfa_score_desc %zu\nfa_fwd_args %zu\n",
-         sizeof(fa_mask_desc), sizeof(fa_block_mask), sizeof(fa_score_desc), sizeof(fa_fwd_args));
+  printf("fa_mask_desc %zu\nfa_block_mask %zu\nfa_score_desc %zu\nfa_fwd_args %zu\nfa_bwd_args %zu\n",
+         sizeof(fa_mask_desc), sizeof(fa_block_mask), sizeof(fa_score_desc), sizeof(fa_fwd_args),
+         sizeof(fa_bwd_args));
+  F(fa_bwd_args, scale) F(fa_bwd_args, q) F(fa_bwd_args, dout) F(fa_bwd_args, lse) F(fa_bwd_args, delta)
   F(fa_mask_desc, seg_ids) F(fa_mask_desc, table) F(fa_mask_desc, table_batch)
   F(fa_block_mask, kv_num_blocks) F(fa_block_mask, full_kv_indices)
   F(fa_block_mask, mask) F(fa_score_desc, alibi_slopes) F(fa_score_desc, rel_max)
@@ -72,8 +74,9 @@ int main(void) {
     assert got["fa_block_mask"] == ctypes.sizeof(fa.BlockMaskStruct)
     assert got["fa_score_desc"] == ctypes.sizeof(fa.ScoreDesc)
     assert got["fa_fwd_args"] == ctypes.sizeof(fa.FwdArgs)
+    assert got["fa_bwd_args"] == ctypes.sizeof(fa.BwdArgs)
     pairs = {"fa_mask_desc": fa.MaskDesc, "fa_block_mask": fa.BlockMaskStruct,
-             "fa_score_desc": fa.ScoreDesc, "fa_fwd_args": fa.FwdArgs}
+             "fa_score_desc": fa.ScoreDesc, "fa_fwd_args": fa.FwdArgs, "fa_bwd_args": fa.BwdArgs}
     for key, off in got.items():
         if "." in key:
             t, m = key.split(".")
@@ -235,3 +238,29 @@ def test_decode_split_choice(fa):
     assert 1 <= s_short <= 2
     assert s_short <= s_long <= 256
     assert lib.fa_decode_splits(None, ctypes.byref(long_)) == 0
+
+
+def _bwd_args(fa, **kw):
+    a = fa.BwdArgs()
+    a.B, a.Hq, a.Hkv, a.q_len, a.kv_len, a.D = 1, 4, 4, 256, 256, 128
+    a.q = a.k = a.v = a.o = a.dout = a.lse = a.dq = a.dk = a.dv = a.delta = FAKE
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("kw,bmkw,status,text", [
+    ({"D": 96}, {}, "ERR_UNSUPPORTED", b"head dim"),
+    ({"Hkv": 3}, {}, "ERR_INVALID_ARG", b"multiple"),
+    ({"dout": None}, {}, "ERR_INVALID_ARG", b"non-NULL"),
+    ({"o": FAKE + 8}, {}, "ERR_INVALID_ARG", b"16-byte"),
+    ({"dk": FAKE + 4}, {}, "ERR_INVALID_ARG", b"8-byte"),
+    ({"delta": FAKE + 2}, {}, "ERR_INVALID_ARG", b"4-byte"),
+    ({"q_len": 300}, {}, "ERR_INVALID_ARG", b"built for"),
+    ({}, {"H": 2}, "ERR_INVALID_ARG", b"block mask H"),
+])
+def test_bwd_rejects(fa, kw, bmkw, status, text):
+    lib = fa.load_library()
+    st = lib.fa_bwd(ctypes.byref(_bwd_args(fa, **kw)), ctypes.byref(_bm(fa, **bmkw)), None, None)
+    assert st == getattr(fa, status), lib.fa_last_error()
+    assert text in lib.fa_last_error()
