@@ -780,7 +780,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     const int ch = c0 + 64 * h;          // kv index of the half's column 0
                     // the row's table bits of this half, loaded before S is waited for
                     uint32_t tw0 = 0u, tw1 = 0u;
-                    if (partial && tab_row) {
+                    if (partial && tab_row && ch < p.kv_len) {
                         tw0 = __ldg(tab_row + (ch >> 5));
                         if (ch + 32 < p.kv_len) tw1 = __ldg(tab_row + (ch >> 5) + 1);
                     }
@@ -869,8 +869,8 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     if (partial && table) {
                         // a lookup-table mask: bit e of the half's two words
                         // (bits past kv_len ignored)
-                        const int nvalid = p.kv_len - ch;
-                        if (nvalid < 32) tw0 &= (1u << nvalid) - 1u;
+                        const int nvalid = p.kv_len - ch;       // <= 0: the whole half is past kv_len
+                        if (nvalid < 32) tw0 = nvalid <= 0 ? 0u : (tw0 & ((1u << nvalid) - 1u));
                         if (nvalid < 64) tw1 = nvalid <= 32 ? 0u : (tw1 & ((1u << (nvalid - 32)) - 1u));
                         const float off = -CUDART_INF_F;
 #pragma unroll

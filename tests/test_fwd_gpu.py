@@ -200,15 +200,18 @@ def test_repeated_launches_are_bitwise_identical(name):
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
 @pytest.mark.parametrize("D", [64, 128])
-@pytest.mark.parametrize("case", ["tree", "square"])
+@pytest.mark.parametrize("case", ["tree", "tree_short_tail", "square"])
 def test_table_masks(dtype, D, case):
-    """Lookup-table masks: candidate trees behind a 700-token context (tree
-    attention, q_len = tree size) and a random blocky square table; each batch
-    row reads its own table."""
+    """Lookup-table masks: candidate trees behind a context (tree attention,
+    q_len = tree size; in the short-tail case the last kv tile's second half
+    lies wholly past kv_len) and a random blocky square table; each batch row
+    reads its own table."""
     import torch
     from block_sparse_attention_fa_gb300 import fa
     if case == "tree":
         table = synth.tree_table(17, 2, 700, 150)
+    elif case == "tree_short_tail":
+        table = synth.tree_table(18, 2, 500, 60)
     else:
         rng = np.random.default_rng(5)
         coarse = rng.random((2, 6, 6))
