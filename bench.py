@@ -417,6 +417,42 @@ def decode_section(device, flush, steps, warmup, peaks, peak_src):
     return out
 
 
+# ------------------------------------------------------------------- backward
+
+BACKWARD_WORKLOADS = ["causal_softcap_bf16", "window_alibi_softcap_bf16"]
+
+
+def backward_section(device, flush, steps, warmup, peaks, peak_src):
+    """Time fa_bwd (delta, dK/dV and dQ kernels, one CUDA graph replay, L2
+    flushed) after a forward on the same inputs.  Algorithmic FLOPs: 5
+    products per visited tile (S, dP, dV, dK, dQ) = 2.5 x the forward's."""
+    import torch
+    from block_sparse_attention_fa_gb300 import fa
+    out = {}
+    for name in BACKWARD_WORKLOADS:
+        w = synth.WORKLOADS[name]
+        r = Runner(w, device)
+        o, lse = r.fwd()
+        dout = torch.from_numpy(synth.round_to_bf16(synth.standard_normal(w.seed + 500, tuple(r.q.shape)))).to(
+            device).to(torch.bfloat16)
+        f32 = dict(dtype=torch.float32, device=device)
+        dq, dk, dv = torch.empty(r.q.shape, **f32), torch.empty(r.k.shape, **f32), torch.empty(r.v.shape, **f32)
+        delta = torch.empty(lse.shape, **f32)
+        g = r.graph(lambda: fa.bwd(r.q, r.k, r.v, o, lse, dout, r.bm, dq=dq, dk=dk, dv=dv, delta=delta,
+                                   **r.score_kw))
+        ms = statistics.mean(r.time_graph(g, steps, warmup, flush))
+        flops = 2.5 * r.flops
+        tf = flops / (ms * 1e-3) / 1e12
+        out[name] = {"ms": round(ms, 4), "tflops": round(tf, 2),
+                     "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peaks["bf16_tflops"],
+                                  "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4),
+                                  "peak_source": peak_src, "algorithmic_flops": flops,
+                                  "kernels": ["bwd_delta_kernel", "bwd_dkdv_kernel", "bwd_dq_kernel"]}}
+        del r, dq, dk, dv, dout
+        torch.cuda.empty_cache()
+    return out
+
+
 # ----------------------------------------------------------- CPU (oracle) side
 
 def oracle_rate(w, seconds, threads, seed=0, max_rows=None):
@@ -534,6 +570,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--decode-only", action="store_true",
                     help="time only the split-KV decoding workloads and print their section")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -616,6 +653,9 @@ def main():
     decode = None
     if rank == 0 and not args.no_decode:
         decode = decode_section(device, flush, args.steps, args.warmup, peaks, peak_src)
+    backward = None
+    if rank == 0 and not args.no_backward:
+        backward = backward_section(device, flush, max(3, args.steps // 4), args.warmup, peaks, peak_src)
 
     cpu = None
     if rank == 0 and not args.no_cpu:
@@ -653,6 +693,7 @@ def main():
             "peaks": {"source": peak_src, **peaks},
             "workloads": secondary,
             "decode": decode,
+            "backward": backward,
             **extra,
         }
         print(json.dumps(line), flush=True)
