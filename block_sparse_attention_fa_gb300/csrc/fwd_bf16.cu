@@ -325,7 +325,9 @@ struct PairSeq {
     }
 };
 
-template <int D, int SCORE>
+// TABLE: the mask is a lookup table (FA_MASK_TABLE).  A template parameter,
+// so that the other masks' code carries none of the table's loads.
+template <int D, int SCORE, bool TABLE>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -656,7 +658,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const uint32_t tO = tmem + 256u + D * t;
         const float sl2 = p.scale * kLog2e;
         const bool doc = p.mask.kind == FA_MASK_DOCUMENT;
-        const bool table = p.mask.kind == FA_MASK_TABLE;
+        constexpr bool table = TABLE;
         float cap_in = 0.f, cap_out = 0.f, s_lim = 0.f;
         float tq0 = 0.f, tq1 = 0.f, tq2 = 0.f, tq3 = 0.f, tq4 = 0.f;
         if (SCORE == FA_SCORE_SOFTCAP || SCORE == FA_SCORE_ALIBI_SOFTCAP) {
@@ -1052,10 +1054,10 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     }
 }
 
-template <int D, int SCORE>
+template <int D, int SCORE, bool TABLE>
 cudaError_t launch_one(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, cudaStream_t s) {
-    auto kern = fwd_bf16_kernel<D, SCORE>;
+    auto kern = fwd_bf16_kernel<D, SCORE, TABLE>;
     constexpr uint32_t smem = Layout<D>::kDynamic;
     static int configured_dev = -1;
     int dev = 0;
@@ -1081,16 +1083,22 @@ cudaError_t launch_one(const FwdParams& p, const CUtensorMap& tq, const CUtensor
     return cudaGetLastError();
 }
 
+template <int D, bool TABLE>
+cudaError_t launch_dt(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                      const CUtensorMap& tv, cudaStream_t s) {
+    switch (p.score.kind) {
+        case FA_SCORE_SOFTCAP: return launch_one<D, FA_SCORE_SOFTCAP, TABLE>(p, tq, tk, tv, s);
+        case FA_SCORE_ALIBI: return launch_one<D, FA_SCORE_ALIBI, TABLE>(p, tq, tk, tv, s);
+        case FA_SCORE_REL_BIAS: return launch_one<D, FA_SCORE_REL_BIAS, TABLE>(p, tq, tk, tv, s);
+        case FA_SCORE_ALIBI_SOFTCAP: return launch_one<D, FA_SCORE_ALIBI_SOFTCAP, TABLE>(p, tq, tk, tv, s);
+        default: return launch_one<D, FA_SCORE_NONE, TABLE>(p, tq, tk, tv, s);
+    }
+}
+
 template <int D>
 cudaError_t launch_d(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                      const CUtensorMap& tv, cudaStream_t s) {
-    switch (p.score.kind) {
-        case FA_SCORE_SOFTCAP: return launch_one<D, FA_SCORE_SOFTCAP>(p, tq, tk, tv, s);
-        case FA_SCORE_ALIBI: return launch_one<D, FA_SCORE_ALIBI>(p, tq, tk, tv, s);
-        case FA_SCORE_REL_BIAS: return launch_one<D, FA_SCORE_REL_BIAS>(p, tq, tk, tv, s);
-        case FA_SCORE_ALIBI_SOFTCAP: return launch_one<D, FA_SCORE_ALIBI_SOFTCAP>(p, tq, tk, tv, s);
-        default: return launch_one<D, FA_SCORE_NONE>(p, tq, tk, tv, s);
-    }
+    return p.mask.kind == FA_MASK_TABLE ? launch_dt<D, true>(p, tq, tk, tv, s) : launch_dt<D, false>(p, tq, tk, tv, s);
 }
 
 }  // namespace
