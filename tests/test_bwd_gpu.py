@@ -113,3 +113,10 @@ def test_window_alibi_softcap_workload():
     tokens, D 64, window 512, ALiBi then soft-cap)."""
     w = synth.WORKLOADS["window_alibi_softcap_bf16"]
     _run(w)
+
+
+def test_causal_softcap_full_length():
+    """The causal soft-cap workload's sequence length, input scale and cap
+    (T 4096, inputs x2, C 50) on two heads of one batch row, all rows."""
+    w = synth.WORKLOADS["causal_softcap_bf16"].scaled(B=1, Hq=2, Hkv=2)
+    _run(w)
