@@ -395,15 +395,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const BwdParams 
 template <int D, int SCORE>
 cudaError_t launch_bwd_score(const BwdParams& p, cudaStream_t s) {
     constexpr uint32_t smem_kv = 4 * BwdTile<D>::kBytes + 2 * 128 * sizeof(float);
-    static bool attr_set = false;
-    if (!attr_set) {
+    // the shared-memory opt-in is per device: set it on each device once
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaError_t e0 = cudaGetDevice(&dev);
+    if (e0 != cudaSuccess) return e0;
+    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
         cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, SCORE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem_kv);
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(bwd_dq_kernel<D, SCORE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem_kv);
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
     bwd_dkdv_kernel<D, SCORE><<<dim3((unsigned)p.bm.nkv, (unsigned)(p.B * p.Hkv)), kBwdThreads, smem_kv, s>>>(p);
     cudaError_t e = cudaGetLastError();

@@ -471,11 +471,15 @@ template <int D, int SCORE>
 cudaError_t launch_split(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s) {
     auto kern = decode_split_kernel<D, SCORE>;
     constexpr uint32_t smem = DecLayout<D>::kDynamic;
-    static bool attr_set = false;
-    if (!attr_set) {
+    // the shared-memory opt-in is per device: set it on each device once
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaError_t e0 = cudaGetDevice(&dev);
+    if (e0 != cudaSuccess) return e0;
+    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
     const dim3 grid((unsigned)p.splits, (unsigned)p.num_groups);
     kern<<<grid, kDecThreads, smem, s>>>(tk, tv, p);
