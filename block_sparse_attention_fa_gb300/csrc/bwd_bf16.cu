@@ -31,6 +31,7 @@
 
 #include "fa_internal.h"
 #include "ptx.cuh"
+#include "tanh_poly.h"
 
 namespace fa {
 namespace {
@@ -78,6 +79,25 @@ __device__ __forceinline__ void load_tile(uint8_t* dst, const uint16_t* src, int
     }
 }
 
+// The same, with cp.async: the copies land while the previous tile is used.
+// Rows past rows_total are zero-filled (no bytes read; the source address
+// given is the matrix's first row).
+template <int D>
+__device__ __forceinline__ void load_tile_async(uint32_t dst, const uint16_t* src, int row0, int rows_total) {
+    constexpr int kChunks = D / 8;
+    for (int x = threadIdx.x; x < 128 * kChunks; x += kBwdThreads) {
+        const int r = x / kChunks, c = x % kChunks;
+        const bool in = row0 + r < rows_total;
+        const uint16_t* g = src + (size_t)(in ? row0 + r : 0) * D + 8 * c;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst + r * BwdTile<D>::kRow + c * 16),
+                     "l"(g), "r"(in ? 16 : 0)
+                     : "memory");
+    }
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// all but the most recent group of this thread's copies have landed
+__device__ __forceinline__ void cp_async_wait_prev() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
 // mask_mod of a partial tile (built-in predicates and the lookup table).
 __device__ __forceinline__ bool bwd_visible(const BwdParams& p, int b, int i, int j) {
     if (i >= p.q_len || j >= p.kv_len) return false;
@@ -98,12 +118,26 @@ __device__ __forceinline__ bool bwd_visible(const BwdParams& p, int b, int i, in
     }
 }
 
+// tanh(u): the minimax polynomial of tanh_poly.h (relative error 6.9e-6)
+// where |u| <= kTanhRange, CUDA's tanhf beyond.
+__device__ __forceinline__ float bwd_tanh(float u) {
+    if (fabsf(u) <= kTanhRange) {
+        const float w = u * u;
+        float q = fmaf(w, kTanhC4, kTanhC3);
+        q = fmaf(q, w, kTanhC2);
+        q = fmaf(q, w, kTanhC1);
+        q = fmaf(q, w, kTanhC0);
+        return u * q;
+    }
+    return tanhf(u);
+}
+
 // score_mod of the scaled score s and its derivative d score_mod / d s.
 template <int SCORE>
 __device__ __forceinline__ float bwd_score(const BwdParams& p, float s, int hq, int i, int j, float& ds) {
     ds = 1.f;
     if (SCORE == FA_SCORE_SOFTCAP) {
-        const float t = tanhf(s / p.score.softcap);
+        const float t = bwd_tanh(s / p.score.softcap);
         ds = 1.f - t * t;
         return p.score.softcap * t;
     }
@@ -115,7 +149,7 @@ __device__ __forceinline__ float bwd_score(const BwdParams& p, float s, int hq, 
     }
     if (SCORE == FA_SCORE_ALIBI_SOFTCAP) {
         const float u = s - __ldg(p.score.slopes + hq) * fabsf(static_cast<float>(i - j));
-        const float t = tanhf(u / p.score.softcap);
+        const float t = bwd_tanh(u / p.score.softcap);
         ds = 1.f - t * t;
         return p.score.softcap * t;
     }
@@ -160,12 +194,12 @@ template <int D, int SCORE>
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const BwdParams p) {
     using T = BwdTile<D>;
     extern __shared__ __align__(16) uint8_t smem[];
+    // K, V, then two buffers of (Q, dO, lse * log2 e, Delta): the next visited
+    // q-block's tiles are copied while the current one is used
     uint8_t* sK = smem;
     uint8_t* sV = sK + T::kBytes;
-    uint8_t* sQ = sV + T::kBytes;
-    uint8_t* sG = sQ + T::kBytes;                            // dO
-    float* sL = reinterpret_cast<float*>(sG + T::kBytes);    // lse * log2 e (+inf for rows with no key)
-    float* sDelta = sL + 128;
+    constexpr int kBuf = 2 * T::kBytes + 2 * 128 * 4;
+    uint8_t* const sBuf = sV + T::kBytes;
     const int kb = blockIdx.x, g = blockIdx.y;
     const int b = g / p.Hkv, hk = g % p.Hkv;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -177,7 +211,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const BwdParam
     load_tile<D>(sK, kbase, kb * kBlock, p.kv_len);
     load_tile<D>(sV, vbase, kb * kBlock, p.kv_len);
     __syncthreads();
-    const uint32_t aK = smem_addr(sK), aV = smem_addr(sV), aQ = smem_addr(sQ), aG = smem_addr(sG);
+    const uint32_t aK = smem_addr(sK), aV = smem_addr(sV);
     // K and V of the warp's 16 keys as A fragments (rows = keys, k = d)
     uint32_t ka[D / 16][4], va[D / 16][4];
     {
@@ -192,22 +226,48 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const BwdParam
 #pragma unroll
     for (int t = 0; t < D / 8; ++t) dk[t][0] = dk[t][1] = dk[t][2] = dk[t][3] = dv[t][0] = dv[t][1] = dv[t][2] = dv[t][3] = 0.f;
 
-    for (int hq = hk * p.group; hq < (hk + 1) * p.group; ++hq) {
-        const size_t qrow0 = ((size_t)b * p.Hq + hq) * p.q_len;
-        for (int qb = 0; qb < p.bm.nq; ++qb) {
-            const int kind = tile_kind(p, b, hq, qb, kb);  // uniform over the CTA
-            if (kind == 0) continue;
-            const bool partial = kind == 1;
-            __syncthreads();                                   // previous tiles consumed
-            load_tile<D>(sQ, static_cast<const uint16_t*>(p.q) + qrow0 * D, qb * kBlock, p.q_len);
-            load_tile<D>(sG, static_cast<const uint16_t*>(p.dout) + qrow0 * D, qb * kBlock, p.q_len);
-            for (int r = threadIdx.x; r < 128; r += kBwdThreads) {
-                const int i = qb * kBlock + r;
-                const float lse = i < p.q_len ? __ldg(p.lse + qrow0 + i) : -CUDART_INF_F;
-                sL[r] = lse == -CUDART_INF_F ? CUDART_INF_F : lse * kLog2eB;
-                sDelta[r] = i < p.q_len ? __ldg(p.delta + qrow0 + i) : 0.f;
+    // The visited (query head, q-block) pairs in order: from (hq, qb) on, the
+    // next one whose BlockMask row lists this kv block; 0 when none is left.
+    auto advance = [&](int& hq, int& qb) -> int {
+        for (; hq < (hk + 1) * p.group; ++hq, qb = 0)
+            for (; qb < p.bm.nq; ++qb) {
+                const int kind = tile_kind(p, b, hq, qb, kb);
+                if (kind) return kind;
             }
-            __syncthreads();
+        return 0;
+    };
+    // copies of a visit's Q, dO into buffer `buf`, and its lse and Delta
+    auto issue = [&](int buf, int hq, int qb) {
+        uint8_t* base = sBuf + buf * kBuf;
+        const size_t qrow0 = ((size_t)b * p.Hq + hq) * p.q_len;
+        load_tile_async<D>(smem_addr(base), static_cast<const uint16_t*>(p.q) + qrow0 * D, qb * kBlock, p.q_len);
+        load_tile_async<D>(smem_addr(base + T::kBytes), static_cast<const uint16_t*>(p.dout) + qrow0 * D,
+                           qb * kBlock, p.q_len);
+        float* l = reinterpret_cast<float*>(base + 2 * T::kBytes);
+        for (int r = threadIdx.x; r < 128; r += kBwdThreads) {
+            const int i = qb * kBlock + r;
+            const float lse = i < p.q_len ? __ldg(p.lse + qrow0 + i) : -CUDART_INF_F;
+            l[r] = lse == -CUDART_INF_F ? CUDART_INF_F : lse * kLog2eB;   // rows with no key: P = 0
+            l[128 + r] = i < p.q_len ? __ldg(p.delta + qrow0 + i) : 0.f;
+        }
+    };
+    int hq = hk * p.group, qb = 0, buf = 0;
+    int kind = advance(hq, qb);
+    if (kind) issue(0, hq, qb);
+    cp_async_commit();
+    while (kind) {
+        int nhq = hq, nqb = qb + 1;
+        const int nkind = advance(nhq, nqb);
+        if (nkind) issue(buf ^ 1, nhq, nqb);
+        cp_async_commit();
+        cp_async_wait_prev();                                  // this visit's copies have landed
+        __syncthreads();
+        {
+            const bool partial = kind == 1;
+            uint8_t* base = sBuf + buf * kBuf;
+            const uint32_t aQ = smem_addr(base), aG = smem_addr(base + T::kBytes);
+            const float* sL = reinterpret_cast<const float*>(base + 2 * T::kBytes);
+            const float* sDelta = sL + 128;
             // 16 queries at a time: n8 tiles nt = 0, 1
             for (int qc = 0; qc < 128; qc += 16) {
                 float s[2][4] = {}, dp[2][4] = {};
@@ -238,7 +298,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const BwdParam
                             const int i = qb * kBlock + qi, j = key0 + gr + 8 * hh;
                             float dsm;
                             const float sv = bwd_score<SCORE>(p, s[nt][2 * hh + c] * p.scale, hq, i, j, dsm);
-                            float pr = exp2f(fmaf(sv, kLog2eB, -sL[qi]));
+                            float pr = ex2_approx(fmaf(sv, kLog2eB, -sL[qi]));
                             if (j >= p.kv_len || (partial && !bwd_visible(p, b, i, j))) pr = 0.f;
                             pv[c] = pr;
                             dsv[c] = pr * (dp[nt][2 * hh + c] - sDelta[qi]) * dsm;
@@ -263,6 +323,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const BwdParam
                 }
             }
         }
+        __syncthreads();                                       // buffer `buf` is free for the next copies
+        hq = nhq;
+        qb = nqb;
+        kind = nkind;
+        buf ^= 1;
     }
     // write this warp's 16 rows of dK (times scale) and dV
     float* dkb = p.dk + ((size_t)b * p.Hkv + hk) * (size_t)p.kv_len * D;
@@ -285,10 +350,11 @@ template <int D, int SCORE>
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const BwdParams p) {
     using T = BwdTile<D>;
     extern __shared__ __align__(16) uint8_t smem[];
-    uint8_t* sK = smem;
-    uint8_t* sV = sK + T::kBytes;
-    uint8_t* sQ = sV + T::kBytes;
+    // Q, dO, then two buffers of (K, V): the next visited kv tile is copied
+    // while the current one is used
+    uint8_t* sQ = smem;
     uint8_t* sG = sQ + T::kBytes;
+    uint8_t* const sKV = sG + T::kBytes;
     const int qb = blockIdx.x, g = blockIdx.y;
     const int b = g / p.Hq, hq = g % p.Hq, hk = hq / p.group;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -299,7 +365,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const BwdParams 
     load_tile<D>(sQ, static_cast<const uint16_t*>(p.q) + qrow0 * D, qb * kBlock, p.q_len);
     load_tile<D>(sG, static_cast<const uint16_t*>(p.dout) + qrow0 * D, qb * kBlock, p.q_len);
     __syncthreads();
-    const uint32_t aK = smem_addr(sK), aV = smem_addr(sV), aQ = smem_addr(sQ), aG = smem_addr(sG);
+    const uint32_t aQ = smem_addr(sQ), aG = smem_addr(sG);
     uint32_t qa[D / 16][4], ga[D / 16][4];
     {
         const int r = 16 * warp + (lane & 15), cofs = (lane >> 4) * 16;
@@ -325,14 +391,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const BwdParams 
     const int np = __ldg(p.bm.kv_num_blocks + row), nf = __ldg(p.bm.full_kv_num_blocks + row);
     const uint16_t* kbase = static_cast<const uint16_t*>(p.k) + ((size_t)b * p.Hkv + hk) * (size_t)p.kv_len * D;
     const uint16_t* vbase = static_cast<const uint16_t*>(p.v) + ((size_t)b * p.Hkv + hk) * (size_t)p.kv_len * D;
+    auto kv_block = [&](int e) {
+        return e < np ? __ldg(p.bm.kv_indices + row * p.bm.nkv + e)
+                      : __ldg(p.bm.full_kv_indices + row * p.bm.nkv + (e - np));
+    };
+    auto issue = [&](int buf, int kbi) {
+        const uint32_t base = smem_addr(sKV) + buf * 2 * T::kBytes;
+        load_tile_async<D>(base, kbase, kbi * kBlock, p.kv_len);
+        load_tile_async<D>(base + T::kBytes, vbase, kbi * kBlock, p.kv_len);
+    };
+    if (np + nf > 0) issue(0, kv_block(0));
+    cp_async_commit();
     for (int e = 0; e < np + nf; ++e) {
         const bool partial = e < np;
-        const int kb = partial ? __ldg(p.bm.kv_indices + row * p.bm.nkv + e)
-                               : __ldg(p.bm.full_kv_indices + row * p.bm.nkv + (e - np));
+        const int kb = kv_block(e);
+        const int buf = e & 1;
+        if (e + 1 < np + nf) issue(buf ^ 1, kv_block(e + 1));
+        cp_async_commit();
+        cp_async_wait_prev();                                  // tile e has landed
         __syncthreads();
-        load_tile<D>(sK, kbase, kb * kBlock, p.kv_len);
-        load_tile<D>(sV, vbase, kb * kBlock, p.kv_len);
-        __syncthreads();
+        const uint32_t aK = smem_addr(sKV) + buf * 2 * T::kBytes, aV = aK + T::kBytes;
         for (int kc = 0; kc < 128; kc += 16) {
             float s[2][4] = {}, dp[2][4] = {};
             {
@@ -359,7 +437,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const BwdParams 
                         const int i = r0 + gr + 8 * hh, j = kb * kBlock + kc + 8 * nt + 2 * tq + c;
                         float dsm;
                         const float sv = bwd_score<SCORE>(p, s[nt][2 * hh + c] * p.scale, hq, i, j, dsm);
-                        float pr = exp2f(fmaf(sv, kLog2eB, -lse2[hh]));
+                        float pr = ex2_approx(fmaf(sv, kLog2eB, -lse2[hh]));
                         if (i >= p.q_len || j >= p.kv_len || (partial && !bwd_visible(p, b, i, j))) pr = 0.f;
                         dsv[c] = pr * (dp[nt][2 * hh + c] - dl[hh]) * dsm;
                     }
@@ -378,6 +456,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const BwdParams 
                 }
             }
         }
+        __syncthreads();                                       // buffer `buf` is free for the next copies
     }
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
@@ -394,7 +473,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const BwdParams 
 
 template <int D, int SCORE>
 cudaError_t launch_bwd_score(const BwdParams& p, cudaStream_t s) {
-    constexpr uint32_t smem_kv = 4 * BwdTile<D>::kBytes + 2 * 128 * sizeof(float);
+    // dK/dV: K, V and two buffers of (Q, dO, lse, Delta); dQ: Q, dO and two
+    // buffers of (K, V)
+    constexpr uint32_t smem_kv = 6 * BwdTile<D>::kBytes + 4 * 128 * sizeof(float);
     // the shared-memory opt-in is per device: set it on each device once
     static bool attr_set[64] = {};
     int dev = 0;
