@@ -54,14 +54,19 @@ namespace {
 
 constexpr int kThreads = 384;   // warpgroups 0-1: softmax; warpgroup 2: loader, 2 MMA, 1 idle
 // Registers per thread: one CTA per SM is launched with 168 (65536 / 384,
-// rounded down to 8); warpgroup 2 gives 48 of them to the two softmax
-// warpgroups: 4 x 32 x (192 + 192 + 120) = 384 x 168.  build.py checks the
-// launch count.
+// rounded down to 8); warpgroup 2 gives part of its share to the two softmax
+// warpgroups: 4 x 32 x (S + S + X) = 384 x 168.  The loader and MMA warps fit
+// in 88.  With D = 128 the softmax takes 208 (2-3 % faster on the causal
+// soft-cap and window workloads than 192); with D = 64 192 measured better.
+// build.py checks the launch count.
 constexpr uint32_t kRegsLaunch = 168;
-constexpr uint32_t kRegsSoftmax = 192;
-constexpr uint32_t kRegsOther = 120;
-static_assert(128 * (2 * kRegsSoftmax + kRegsOther) == kThreads * kRegsLaunch,
-              "register split must match the launch");
+template <int D>
+struct RegSplit {
+    static constexpr uint32_t kSoftmax = D == 128 ? 208 : 192;
+    static constexpr uint32_t kOther = (kThreads / 128) * kRegsLaunch - 2 * kSoftmax;
+    static_assert(128 * (2 * kSoftmax + kOther) == kThreads * kRegsLaunch, "register split must match the launch");
+    static_assert(kSoftmax % 8 == 0 && kOther % 8 == 0 && kOther >= 88, "setmaxnreg counts");
+};
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -378,7 +383,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
     if (warp >= 8) {
     // Warpgroup 2 hands registers to the softmax warpgroups first thing.
-    regs_decrease<kRegsOther>();
+    regs_decrease<RegSplit<D>::kOther>();
     if (warp == 8) {
         // ------------------------------------------------------------ loader
         if (lane == 0) {
@@ -648,7 +653,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     }
     } else {
         // ----------------------------------------------------------- softmax
-        regs_increase<kRegsSoftmax>();
+        regs_increase<RegSplit<D>::kSoftmax>();
         const int t = warp >> 2;                    // query tile of this warpgroup
         const int wq = warp & 3;                    // its 32 rows: TMEM lanes 32 wq ..
         const int r = wq * 32 + lane;
