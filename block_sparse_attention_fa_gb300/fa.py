@@ -379,6 +379,11 @@ def fwd_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, bm: BlockMask,
         out = torch.empty(q.shape, dtype=torch.float32 if out_fp32 else q.dtype, device=q.device)
     if lse is None:
         lse = torch.empty((B, Hq, Tq), dtype=torch.float32, device=q.device)
+    want = torch.float32 if out_fp32 else torch.bfloat16
+    if out.dtype != want or not out.is_cuda or not out.is_contiguous() or tuple(out.shape) != tuple(q.shape):
+        raise ValueError(f"out must be a contiguous CUDA {want} tensor of q's shape")
+    if lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous() or tuple(lse.shape) != (B, Hq, Tq):
+        raise ValueError("lse must be a contiguous CUDA float32 tensor [B, Hq, q_len]")
     a = decode_args(q, k, out, lse, v=v, scale=scale, out_fp32=out_fp32)
     a.timeout_ms = timeout_ms
     lib = load_library()
@@ -386,6 +391,8 @@ def fwd_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, bm: BlockMask,
         num_splits = int(lib.fa_decode_splits(ctypes.byref(a), ctypes.byref(bm.struct))) or 1
     if partials is None:
         partials = decode_partials(q, num_splits)
+    if partials.dtype != torch.float32 or not partials.is_cuda or not partials.is_contiguous():
+        raise ValueError("partials must be a contiguous CUDA float32 tensor (see decode_partials)")
     sc = _score_desc(score, softcap, alibi_slopes, rel_bias, rel_max)
     ws = workspace or default_workspace(q.device, stream)
     _check(lib.fa_fwd_decode(ctypes.byref(a), ctypes.byref(bm.struct), ctypes.byref(sc), num_splits,
@@ -406,11 +413,17 @@ def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse:
             raise ValueError("q, k, v, o and dout must be contiguous CUDA bf16 tensors [B, H, T, D]")
     B, Hq, Tq, D = q.shape
     Hkv, Tkv = k.shape[1], k.shape[2]
+    if tuple(o.shape) != tuple(q.shape) or tuple(dout.shape) != tuple(q.shape):
+        raise ValueError("o and dout must have q's shape")
     f32 = dict(dtype=torch.float32, device=q.device)
     dq = torch.empty((B, Hq, Tq, D), **f32) if dq is None else dq
     dk = torch.empty((B, Hkv, Tkv, D), **f32) if dk is None else dk
     dv = torch.empty((B, Hkv, Tkv, D), **f32) if dv is None else dv
     delta = torch.empty((B, Hq, Tq), **f32) if delta is None else delta
+    for name, t, shape in (("lse", lse, (B, Hq, Tq)), ("dq", dq, (B, Hq, Tq, D)), ("dk", dk, (B, Hkv, Tkv, D)),
+                           ("dv", dv, (B, Hkv, Tkv, D)), ("delta", delta, (B, Hq, Tq))):
+        if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous() or tuple(t.shape) != shape:
+            raise ValueError(f"{name} must be a contiguous CUDA float32 tensor of shape {shape}")
     a = BwdArgs()
     a.B, a.Hq, a.Hkv, a.q_len, a.kv_len, a.D = B, Hq, Hkv, Tq, Tkv, D
     a.scale = 0.0 if scale is None else float(scale)

@@ -264,3 +264,16 @@ def test_bwd_rejects(fa, kw, bmkw, status, text):
     st = lib.fa_bwd(ctypes.byref(_bwd_args(fa, **kw)), ctypes.byref(_bm(fa, **bmkw)), None, None)
     assert st == getattr(fa, status), lib.fa_last_error()
     assert text in lib.fa_last_error()
+
+
+def test_binding_rejects_wrong_tensors_before_the_library(fa):
+    """The Python wrappers check dtypes and shapes of what they pass on (CPU
+    tensors here: the check fails before any CUDA call)."""
+    import torch
+    q = torch.zeros((1, 2, 4, 64), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.bwd(q, q, q, q, torch.zeros(1), q, None)
+    with pytest.raises(ValueError):
+        fa.fwd_decode(q, q, q, None)
+    with pytest.raises(ValueError):
+        fa.fwd_decode(q.float(), q, q, None)
