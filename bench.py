@@ -81,6 +81,33 @@ def visited_flops(w, bm_np):
     return 4.0 * w.D * total * reps
 
 
+def build_bytes(Bm, Hm, nq, nkv, T, mask, table_bytes=0):
+    """Bytes the BlockMask builder must move at least: the four arrays
+    written (two [Bm, Hm, nq, nkv] index arrays and two [Bm, Hm, nq] counts,
+    int32) and the mask's own data read once (segment ids or the table)."""
+    written = 2 * 4 * Bm * Hm * nq * nkv + 2 * 4 * Bm * Hm * nq
+    read = 4 * Bm * T if mask == "document" else table_bytes
+    return written + read
+
+
+def build_roofline(build_ms, nbytes, peaks, peak_src):
+    gbs = nbytes / (build_ms * 1e-3) / 1e9
+    return {"bound": "hbm", "build_ms": round(build_ms, 4), "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes": nbytes,
+            "peak_source": peak_src, "kernel": "block_mask_kernel"}
+
+
+def tcgen05_peak_tflops(device, sm_mhz):
+    """The tensor pipe's issue rate: 8192 dense bf16 FLOP per clock per SM
+    (128 x 256 x 16 MMA in 128 cycles, measured by a tcgen05 probe) at the SM
+    clock sampled during the timed region."""
+    import torch
+    if not sm_mhz:
+        return None
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    return sms * 8192 * sm_mhz * 1e6 / 1e12
+
+
 def algorithmic_bytes(w):
     """Bytes the forward must move at least: Q, K, V read, O and lse written."""
     el = 2 if w.dtype == "bf16" else 4
@@ -226,6 +253,12 @@ class Runner:
         self.ws.check()
         return [a.elapsed_time(c) for a, c in evs]
 
+    def time_build(self, steps, warmup, flush):
+        """fa_block_mask_build alone (one CUDA graph replay per step, L2
+        flushed before each): per-step times in ms."""
+        g = self.graph(lambda: self.bm.rebuild(workspace=self.ws))
+        return self.time_graph(g, steps, warmup, flush)
+
     def time_steps(self, steps, warmup, flush):
         """(step times, forward-kernel times) in ms: a step is BlockMask build
         + forward; the forward is also timed alone (the dominant kernel)."""
@@ -274,7 +307,7 @@ class Runner:
         return sec, h2d, d2h
 
 
-KERNEL_SOURCES = ["fwd_bf16.cu", "fa_api.cu", "ptx.cuh", "fa_internal.h", "exp2_poly.h", "tanh_poly.h"]
+KERNEL_SOURCES = ["fwd_bf16.cu", "fa_api.cu", "ptx.cuh", "fa_internal.h", "tanh_poly.h"]
 
 
 def kernel_source_digest():
@@ -302,7 +335,7 @@ def measured_traffic(workload):
     return int(t["read"]) + int(t["write"])
 
 
-def summarize(w, r, step_ms, fwd_ms, peaks, peak_src):
+def summarize(w, r, step_ms, fwd_ms, peaks, peak_src, build_ms=None, floor_ms=None):
     ms = statistics.median(step_ms)
     fms = statistics.mean(fwd_ms)
     tflops = r.flops / (ms * 1e-3) / 1e12
@@ -313,8 +346,13 @@ def summarize(w, r, step_ms, fwd_ms, peaks, peak_src):
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
     intensity = r.flops / bytes_
     if w.dtype == "fp32":
-        roof = {"bound": "latency", "achieved": round(fms * 1e3, 2), "peak": None, "unit": "us",
-                "frac": None, "traffic": None}
+        # a latency-bound launch: its floor is the time of one graph-launched
+        # kernel that does nothing measurable, taken in the same run
+        fl = floor_ms if floor_ms else None
+        roof = {"bound": "latency", "achieved": round(fms * 1e3, 2),
+                "peak": round(fl * 1e3, 2) if fl else None, "unit": "us",
+                "frac": round(fl / fms, 4) if fl else None, "traffic": None,
+                "floor": "one-element add kernel replayed from a CUDA graph, same run"}
     elif intensity < ridge:
         roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": None}
@@ -341,6 +379,102 @@ def summarize(w, r, step_ms, fwd_ms, peaks, peak_src):
     }
     if w.groups:
         out["windows_per_s"] = round(w.groups * w.B / (ms * 1e-3), 1)
+    if build_ms is not None:
+        bmn = r.bm_np
+        Bm, Hm, nq = bmn["kv_num_blocks"].shape
+        nkv = bmn["kv_indices"].shape[-1]
+        out["build"] = build_roofline(statistics.mean(build_ms), build_bytes(Bm, Hm, nq, nkv, w.T, w.mask),
+                                      peaks, peak_src)
+    return out
+
+
+def compact(entry, tc_peak):
+    """The few numbers of a workload the last lines of the output keep."""
+    roof = entry["roofline"]
+    c = {"fwd_ms": entry["fwd_ms"], "bound": roof["bound"], "frac": roof["frac"]}
+    if roof["bound"] == "tensor" and tc_peak:
+        c["frac_tcgen05"] = round(roof["achieved"] / tc_peak, 4)
+    if "build" in entry:
+        c["build_ms"] = entry["build"]["build_ms"]
+        c["build_frac"] = entry["build"]["frac"]
+    return c
+
+
+def launch_floor_ms(device, steps, warmup, flush):
+    """CUDA-event time of one graph replay holding one trivial kernel: the
+    launch floor of any single-kernel step on this GPU."""
+    import torch
+    x = torch.zeros(1, device=device)
+    side = torch.cuda.Stream(device=device)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        x.add_(1.0)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        x.add_(1.0)
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, c in evs:
+        flush.zero_()
+        a.record(stream)
+        g.replay()
+        c.record(stream)
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(c) for a, c in evs)
+
+
+# ---------------------------------------------------- the builder at scale
+
+# A BlockMask large enough that its writes leave L2 (129 MB): document masks
+# over 16 packed rows of 131072 tokens (documents of 256-2048 tokens, the
+# document workload's recipe), nq = nkv = 1024, 134 MB of index arrays.
+BUILD_SCALE = {"B": 16, "T": 131072, "seed": 41}
+
+
+def build_scale_section(device, flush, steps, warmup, peaks, peak_src):
+    import torch
+    from block_sparse_attention_fa_gb300 import fa
+    B, T = BUILD_SCALE["B"], BUILD_SCALE["T"]
+    seg = torch.from_numpy(synth.document_segments(BUILD_SCALE["seed"], B, T)).to(device)
+    ws = fa.Workspace(device)
+    bm = fa.block_mask("document", B, 1, T, T, seg_ids=seg, workspace=ws)
+    ws.check()
+
+    def fn():
+        bm.rebuild(workspace=ws)
+
+    side = torch.cuda.Stream(device=device)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()
+        fn()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, c in evs:
+        flush.zero_()
+        a.record(stream)
+        g.replay()
+        c.record(stream)
+    torch.cuda.synchronize()
+    ws.check()
+    ms = statistics.mean(a.elapsed_time(c) for a, c in evs)
+    out = build_roofline(ms, build_bytes(B, 1, bm.nq, bm.nkv, T, "document"), peaks, peak_src)
+    out["config"] = {"mask": "document", "B": B, "T": T, "nq": bm.nq, "nkv": bm.nkv}
+    del bm, seg
+    torch.cuda.empty_cache()
     return out
 
 
@@ -520,7 +654,6 @@ def run_reference(args, w):
     if rank != 0:
         return
     import oracle
-    from block_sparse_attention_fa_gb300 import fa as _fa  # noqa: F401  (not used: CPU only)
     threads = oracle.default_threads()
     # visited FLOPs from the oracle's own tile scan (no GPU involved)
     seg = w.segments()
@@ -611,7 +744,13 @@ def main():
         worst = max_over_ranks(statistics.median(step_ms))
         dist.barrier()
         step_ms = [worst] * len(step_ms)
-    head = summarize(w, r, step_ms, fwd_ms, peaks, peak_src)
+    build_ms = r.time_build(args.steps, args.warmup, flush)
+    floor_ms = launch_floor_ms(device, args.steps, args.warmup, flush)
+    head = summarize(w, r, step_ms, fwd_ms, peaks, peak_src, build_ms=build_ms, floor_ms=floor_ms)
+    clocks = clk.summary()
+    tc_peak = tcgen05_peak_tflops(device, clocks.get("sm_mhz"))
+    if head["roofline"]["bound"] == "tensor" and tc_peak:
+        head["roofline"]["frac_tcgen05"] = round(head["roofline"]["achieved"] / tc_peak, 4)
 
     extra = {}
     if rank == 0 and w.name == "grouped_bf16":
@@ -646,7 +785,11 @@ def main():
             w2 = synth.WORKLOADS[name]
             r2 = Runner(w2, device)
             s2, f2 = r2.time_steps(args.steps, args.warmup, flush)
-            secondary[name] = summarize(w2, r2, s2, f2, peaks, peak_src)
+            b2 = r2.time_build(args.steps, args.warmup, flush)
+            secondary[name] = summarize(w2, r2, s2, f2, peaks, peak_src, build_ms=b2, floor_ms=floor_ms)
+            if secondary[name]["roofline"]["bound"] == "tensor" and tc_peak:
+                roof = secondary[name]["roofline"]
+                roof["frac_tcgen05"] = round(roof["achieved"] / tc_peak, 4)
             del r2
             torch.cuda.empty_cache()
 
@@ -657,12 +800,28 @@ def main():
     if rank == 0 and not args.no_backward:
         backward = backward_section(device, flush, max(3, args.steps // 4), args.warmup, peaks, peak_src)
 
+    build_scale = None
+    if rank == 0 and not args.no_secondary:
+        build_scale = build_scale_section(device, flush, args.steps, args.warmup, peaks, peak_src)
+
     cpu = None
     if rank == 0 and not args.no_cpu:
         cpu = cpu_baseline(w, r.flops, args.cpu_seconds)
 
     if rank == 0:
         n = world
+        # The last keys are the compact per-workload summary, so that the
+        # tail of the line holds every configuration's roofline fraction.
+        summary = {w.name: compact(head, tc_peak)}
+        for name, entry in secondary.items():
+            summary[name] = compact(entry, tc_peak)
+        if build_scale:
+            summary["block_mask_build_16x131072"] = {"build_ms": build_scale["build_ms"],
+                                                      "bound": "hbm", "frac": build_scale["frac"]}
+        for name, entry in (backward or {}).items():
+            summary["bwd_" + name] = {"ms": entry["ms"], "bound": "tensor", "frac": entry["roofline"]["frac"]}
+        for name, entry in (decode or {}).items():
+            summary[name] = {"ms": entry["ms"], "bound": "hbm", "frac": entry["roofline"]["frac"]}
         line = {
             "metric": METRIC,
             "value": round(head["tflops"] * n, 3),
@@ -686,15 +845,20 @@ def main():
             "fwd_ms": head["fwd_ms"],
             "fwd_tflops": head["fwd_tflops"],
             "roofline": head["roofline"],
+            "build": head.get("build"),
             "e2e": e2e,
             "cpu_baseline": cpu,
             "gpu_launches": 2 * args.steps,
-            "clocks": clk.summary(),
-            "peaks": {"source": peak_src, **peaks},
-            "workloads": secondary,
+            "clocks": clocks,
+            "peaks": {"source": peak_src, **peaks, "tcgen05_issue_tflops": tc_peak and round(tc_peak, 1),
+                      "note": "frac: of the measured peaks (cuBLAS bf16 burst, HBM copy); "
+                              "frac_tcgen05: of SMs x 8192 FLOP/clk x the sampled SM clock"},
+            **extra,
             "decode": decode,
             "backward": backward,
-            **extra,
+            "build_at_scale": build_scale,
+            "workloads": secondary,
+            "summary": summary,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -235,6 +235,16 @@ fa_status fa::report(fa_status st, const char* msg) {
     return st;
 }
 
+fa_status fa::fwd_validate(const fa_fwd_args* a, const fa_block_mask* bm, const fa_score_desc* sc,
+                           void* workspace) {
+    fa_status st = check_fwd_args(a, bm, workspace);
+    if (st != FA_OK) return st;
+    const long long units = (long long)a->B * a->Hq * bm->nq;
+    if (units * 2 > 2147483647LL) return fail(FA_ERR_UNSUPPORTED, "too many work units (%lld)", units);
+    fa_score_desc score;
+    return check_score(sc, &score);
+}
+
 extern "C" {
 
 const char* fa_last_error(void) { return g_last_error.c_str(); }
@@ -251,6 +261,15 @@ fa_status fa_block_mask_shape(int32_t B, int32_t H, int32_t q_len, int32_t kv_le
     if (nq) *nq = a;
     if (nkv) *nkv = c;
     if (index_elems) *index_elems = (int64_t)B * H * a * c;
+    return ok();
+}
+
+fa_status fa_block_mask_size(int32_t B, int32_t H, int32_t q_len, int32_t kv_len, int32_t* nq, int32_t* nkv,
+                             size_t* bytes_per_array) {
+    int64_t elems = 0;
+    fa_status st = fa_block_mask_shape(B, H, q_len, kv_len, nq, nkv, &elems);
+    if (st != FA_OK) return st;
+    if (bytes_per_array) *bytes_per_array = (size_t)elems * sizeof(int32_t);
     return ok();
 }
 

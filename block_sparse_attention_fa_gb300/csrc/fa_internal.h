@@ -113,6 +113,10 @@ struct BuildParams {
 // Sets this thread's fa_last_error() message and returns `st`.
 fa_status report(fa_status st, const char* msg);
 
+// Every synchronous check fa_fwd makes on its arguments, without launching
+// anything (FA_OK or the status fa_fwd would return, with its message).
+fa_status fwd_validate(const fa_fwd_args* a, const fa_block_mask* bm, const fa_score_desc* sc, void* workspace);
+
 // Launchers (return the launch's cudaError_t).
 cudaError_t launch_block_mask_build(const BuildParams& p, cudaStream_t s);
 cudaError_t launch_fwd_fp32(const FwdParams& p, cudaStream_t s);

@@ -44,7 +44,6 @@
 #include <climits>
 #include <math_constants.h>
 
-#include "exp2_poly.h"
 #include "tanh_poly.h"
 #include "fa_internal.h"
 #include "ptx.cuh"
@@ -99,28 +98,6 @@ constexpr int kUnitWords = 14;
 // UW_ROW + 6 t + {n_part, n_full, part[n_part - 1], part[n_part - 2], full[n_full - 1], full[n_full - 2]}
 enum UnitWord { UW_UNIT = 0, UW_HAS_STEPS = 1, UW_ROW = 2 };
 
-// Which columns of a full tile take their exponential on the FMA pipe (the
-// polynomial below) instead of the MUFU ex2 unit: columns with
-// (col % 16) < kPolyCols.  0 = all on MUFU.
-constexpr int kPolyCols = 0;
-
-// 2^a for two values on the FMA pipe, a >= -125: a = n + f with n an integer
-// (rounded by adding 1.5 * 2^23) and f in [-1/2, 1/2]; 2^f by the cubic of
-// exp2_poly.h; n is added straight into the exponent field.
-__device__ __forceinline__ void exp2_poly2(float& p0, float& p1, float a0, float a1) {
-    constexpr float kShift = 12582912.0f;
-    float t0, t1, n0, n1, f0, f1, q0, q1;
-    fadd2(t0, t1, a0, a1, kShift, kShift);
-    fadd2(n0, n1, t0, t1, -kShift, -kShift);
-    ffma2(f0, f1, n0, n1, -1.f, -1.f, a0, a1);
-    ffma2(q0, q1, f0, f1, kExp2C3, kExp2C3, kExp2C2, kExp2C2);
-    ffma2(q0, q1, q0, q1, f0, f1, kExp2C1, kExp2C1);
-    ffma2(q0, q1, q0, q1, f0, f1, kExp2C0, kExp2C0);
-    // q + (round(a) << 23): one integer multiply-add per value
-    p0 = __uint_as_float(__float_as_uint(t0) * (1u << 23) + __float_as_uint(q0));
-    p1 = __uint_as_float(__float_as_uint(t1) * (1u << 23) + __float_as_uint(q1));
-}
-
 // d = a * b on two lanes at once.
 __device__ __forceinline__ void fmul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
     ffma2(d0, d1, a0, a1, b0, b1, -0.f, -0.f);
@@ -160,17 +137,12 @@ __device__ __forceinline__ void seg_bounds(const int* a, int key, int& below, in
     upto = bu < 8 ? 16 * bu + cu : 128;
 }
 
-// One pair of probabilities: p = 2^(x * sc - m), by MUFU or by polynomial.
-template <bool POLY>
+// One pair of probabilities: p = 2^(x * sc - m) on the MUFU ex2 unit.
 __device__ __forceinline__ void exp_pair(float& p0, float& p1, float x0, float x1, float sc, float nm) {
     float a0, a1;
     ffma2(a0, a1, x0, x1, sc, sc, nm, nm);
-    if (POLY) {
-        exp2_poly2(p0, p1, fmaxf(a0, -125.f), fmaxf(a1, -125.f));
-    } else {
-        p0 = ex2_approx(a0);
-        p1 = ex2_approx(a1);
-    }
+    p0 = ex2_approx(a0);
+    p1 = ex2_approx(a1);
 }
 
 template <int D>
@@ -939,7 +911,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         for (int e = 0; e < 16; ++e) {
                             const int col = 32 * c + 2 * e;
                             float p0, p1;
-                            exp_pair<false>(p0, p1, x[col], x[col + 1], sc, nm);
+                            exp_pair(p0, p1, x[col], x[col + 1], sc, nm);
                             const int a2 = (e & 1) * 2;
                             fadd2(rs[a2], rs[a2 + 1], rs[a2], rs[a2 + 1], p0, p1);
                             pk[e] = pack_bf16x2(p0, p1);

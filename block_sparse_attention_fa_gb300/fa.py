@@ -24,7 +24,7 @@ OUT_FP32 = 1
 DEBUG_DROP_FIRST_LOAD = 1
 BLOCK = 128
 
-SYMBOLS = ("fa_workspace_bytes", "fa_block_mask_shape", "fa_block_mask_build", "fa_fwd",
+SYMBOLS = ("fa_workspace_bytes", "fa_block_mask_shape", "fa_block_mask_size", "fa_block_mask_build", "fa_fwd",
            "fa_fwd_noalloc", "fa_fwd_decode", "fa_decode_partials_bytes", "fa_decode_splits", "fa_bwd",
            "fa_workspace_check", "fa_last_error", "fa_version")
 
@@ -90,6 +90,9 @@ def load_library(path: str = LIB_PATH):
     h.fa_block_mask_shape.restype = ctypes.c_int
     h.fa_block_mask_shape.argtypes = [ctypes.c_int32] * 4 + [ctypes.POINTER(ctypes.c_int32)] * 2 + \
         [ctypes.POINTER(ctypes.c_int64)]
+    h.fa_block_mask_size.restype = ctypes.c_int
+    h.fa_block_mask_size.argtypes = [ctypes.c_int32] * 4 + [ctypes.POINTER(ctypes.c_int32)] * 2 + \
+        [ctypes.POINTER(ctypes.c_size_t)]
     h.fa_block_mask_build.restype = ctypes.c_int
     h.fa_block_mask_build.argtypes = [ctypes.POINTER(BlockMaskStruct), ctypes.c_void_p, ctypes.c_void_p]
     h.fa_fwd.restype = ctypes.c_int
@@ -236,8 +239,11 @@ def block_mask(mask: str, B: int, H: int, q_len: int, kv_len: int, *, window: in
     if seg_ids is not None:
         if seg_ids.dim() == 1:
             seg_ids = seg_ids[None]
-        if seg_ids.dtype != torch.int32 or not seg_ids.is_cuda:
-            raise ValueError("seg_ids must be a CUDA int32 tensor")
+        if seg_ids.dtype != torch.int32 or not seg_ids.is_cuda or seg_ids.dim() != 2:
+            raise ValueError("seg_ids must be a CUDA int32 tensor [seg_batch, kv_len]")
+        if seg_ids.shape[1] != kv_len or seg_ids.shape[0] not in (1, B):
+            raise ValueError(f"seg_ids must hold kv_len={kv_len} ids per row and 1 or B={B} rows "
+                             f"(got {tuple(seg_ids.shape)})")
         seg_ids = seg_ids.contiguous()
         device = seg_ids.device
     device = torch.device(device or "cuda")
@@ -245,6 +251,42 @@ def block_mask(mask: str, B: int, H: int, q_len: int, kv_len: int, *, window: in
     ws = workspace or default_workspace(device, stream)
     _check(load_library().fa_block_mask_build(ctypes.byref(bm.struct), ws.ptr, _stream_ptr(stream)))
     return bm
+
+
+def _check_fwd_tensors(q, k, v, out, lse, out_fp32, alibi_slopes, rel_bias, rel_max, bm):
+    """The shapes, dtypes and placement fa_fwd / fa_fwd_noalloc read and write
+    through raw pointers, which the C ABI cannot see: anything wrong here
+    would become an out-of-bounds device access, so it is rejected first."""
+    if q.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    for t in (k, v):
+        if t.dtype != q.dtype:
+            raise ValueError("q, k and v must share a dtype")
+    for t in (q, k, v):
+        if not (t.is_cuda and t.is_contiguous() and t.dim() == 4):
+            raise ValueError("q, k, v must be contiguous CUDA tensors [B, H, T, D]")
+    B, Hq, Tq, D = q.shape
+    if tuple(k.shape) != tuple(v.shape):
+        raise ValueError("k and v must have the same shape")
+    if k.shape[0] != B or k.shape[3] != D:
+        raise ValueError("k and v must be [B, Hkv, kv_len, D] with q's B and D")
+    if out_fp32 and q.dtype != torch.bfloat16:
+        raise ValueError("out_fp32 applies to bf16 inputs only")
+    want = torch.float32 if (out_fp32 or q.dtype == torch.float32) else torch.bfloat16
+    if out.dtype != want or not out.is_cuda or not out.is_contiguous() or tuple(out.shape) != tuple(q.shape):
+        raise ValueError(f"out must be a contiguous CUDA {want} tensor of q's shape")
+    if lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous() or tuple(lse.shape) != (B, Hq, Tq):
+        raise ValueError("lse must be a contiguous CUDA float32 tensor [B, Hq, q_len]")
+    if alibi_slopes is not None:
+        if alibi_slopes.dtype != torch.float32 or not alibi_slopes.is_cuda or not alibi_slopes.is_contiguous() \
+                or alibi_slopes.numel() < Hq:
+            raise ValueError("alibi_slopes must be a contiguous CUDA float32 tensor of at least Hq entries")
+    if rel_bias is not None:
+        if rel_bias.dtype != torch.float32 or not rel_bias.is_cuda or not rel_bias.is_contiguous() \
+                or rel_bias.numel() < Hq * (2 * rel_max + 1):
+            raise ValueError("rel_bias must be a contiguous CUDA float32 tensor [Hq, 2 rel_max + 1]")
+    if bm.q_len != Tq or bm.kv_len != k.shape[2]:
+        raise ValueError(f"the BlockMask was built for ({bm.q_len}, {bm.kv_len}), not ({Tq}, {k.shape[2]})")
 
 
 def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, bm: BlockMask, *, score: str = "none",
@@ -256,24 +298,18 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, bm: BlockMask, *, sco
     """Block-sparse attention forward (fa_fwd); returns (o, lse).
 
     ``out_fp32`` writes O in fp32 for bf16 inputs (FA_OUT_FP32)."""
-    if q.dtype == torch.bfloat16:
-        dt = BF16
-    elif q.dtype == torch.float32:
-        dt = FP32
-    else:
+    dt = {torch.bfloat16: BF16, torch.float32: FP32}.get(q.dtype)
+    if dt is None:
         raise ValueError(f"unsupported dtype {q.dtype}")
-    for t in (k, v):
-        if t.dtype != q.dtype:
-            raise ValueError("q, k and v must share a dtype")
-    for t in (q, k, v):
-        if not (t.is_cuda and t.is_contiguous() and t.dim() == 4):
-            raise ValueError("q, k, v must be contiguous CUDA tensors [B, H, T, D]")
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q, k, v must be [B, H, T, D]")
     B, Hq, Tq, D = q.shape
     Hkv, Tkv = k.shape[1], k.shape[2]
     if out is None:
         out = torch.empty(q.shape, dtype=torch.float32 if out_fp32 else q.dtype, device=q.device)
     if lse is None:
         lse = torch.empty((B, Hq, Tq), dtype=torch.float32, device=q.device)
+    _check_fwd_tensors(q, k, v, out, lse, out_fp32, alibi_slopes, rel_bias, rel_max, bm)
     a = FwdArgs()
     a.dtype, a.B, a.Hq, a.Hkv, a.q_len, a.kv_len, a.D = dt, B, Hq, Hkv, Tq, Tkv, D
     a.scale = 0.0 if scale is None else float(scale)
@@ -304,6 +340,7 @@ def fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, bm: BlockMask
     dt = {torch.bfloat16: BF16, torch.float32: FP32}.get(q.dtype)
     if dt is None:
         raise ValueError(f"unsupported dtype {q.dtype}")
+    _check_fwd_tensors(q, k, v, out, lse, out_fp32, alibi_slopes, rel_bias, rel_max, bm)
     B, Hq, Tq, D = q.shape
     a = FwdArgs()
     a.dtype, a.B, a.Hq, a.Hkv, a.q_len, a.kv_len, a.D = dt, B, Hq, k.shape[1], Tq, k.shape[2], D

@@ -184,6 +184,12 @@ size_t fa_workspace_bytes(void);
 fa_status fa_block_mask_shape(int32_t B, int32_t H, int32_t q_len, int32_t kv_len,
                               int32_t *nq, int32_t *nkv, int64_t *index_elems);
 
+/* The same sizes in bytes: nq, nkv and the bytes of EACH of the two index
+ * arrays (kv_indices, full_kv_indices: B * H * nq * nkv int32); the two count
+ * arrays hold B * H * nq int32 each.  Any output pointer may be NULL.       */
+fa_status fa_block_mask_size(int32_t B, int32_t H, int32_t q_len, int32_t kv_len,
+                             int32_t *nq, int32_t *nkv, size_t *bytes_per_array);
+
 /* Build a BlockMask from a built-in mask_mod (create_block_mask).  The caller
  * fills every field of `bm` (B, H, q_len, kv_len, block sizes 128, nq, nkv,
  * the four device buffers and `mask`); the kernel writes the four arrays.
@@ -210,10 +216,18 @@ fa_status fa_fwd(const fa_fwd_args *a, const fa_block_mask *bm, const fa_score_d
  * library holds until the process exits.
  *   - The first call on a device looks up that array's device address
  *     (cudaGetSymbolAddress, with the device current); make that first call
- *     before any stream capture.
- *   - Every call clears the status words on `stream` before its launch.  All
- *     calls share the array, so calls whose work can overlap on the GPU
- *     (unordered streams) race on it.
+ *     before any stream capture.  The lookup is repeated when the device's
+ *     context has changed (after cudaDeviceReset), so that call too should
+ *     come before any capture.
+ *   - Every call clears the array's status words and work-queue counters on
+ *     `stream` before its launch.  All calls share the array, so calls whose
+ *     work can overlap on the GPU (unordered streams) race on it: one call's
+ *     clear resets the other's work queue, the two kernels split or repeat
+ *     each other's work units, and O and lse come out WRONG or unwritten,
+ *     with no error reported.  Order such calls on one stream, or with
+ *     events.
+ *   - A call rejected by the argument checks launches nothing and leaves the
+ *     array untouched.
  *   - A device-side wait that runs out of time still ends the kernel cleanly,
  *     but is not reported here; use fa_fwd with a workspace where that matters.
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.

@@ -31,7 +31,7 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted([
-        "fa_block_mask_build", "fa_block_mask_shape", "fa_bwd", "fa_decode_partials_bytes", "fa_decode_splits", "fa_fwd",
+        "fa_block_mask_build", "fa_block_mask_shape", "fa_block_mask_size", "fa_bwd", "fa_decode_partials_bytes", "fa_decode_splits", "fa_fwd",
         "fa_fwd_decode", "fa_fwd_noalloc", "fa_last_error", "fa_version", "fa_workspace_bytes",
         "fa_workspace_check"])
 
@@ -277,3 +277,35 @@ def test_binding_rejects_wrong_tensors_before_the_library(fa):
         fa.fwd_decode(q, q, q, None)
     with pytest.raises(ValueError):
         fa.fwd_decode(q.float(), q, q, None)
+
+
+def test_binding_rejects_bad_forward_tensors(fa):
+    """fwd and fwd_noalloc share one check of everything they hand to the C
+    ABI as raw pointers (CPU tensors and wrong shapes fail before any CUDA
+    call); so does block_mask for the segment ids."""
+    import torch
+
+    class _BM:
+        q_len, kv_len = 4, 4
+
+    q = torch.zeros((1, 2, 4, 64), dtype=torch.bfloat16)
+    lse = torch.zeros((1, 2, 4))
+    for call in (lambda **kw: fa.fwd(q, q, q, _BM(), **kw),
+                 lambda **kw: fa.fwd_noalloc(q, q, q, _BM(), out=q, lse=lse, **kw)):
+        with pytest.raises(ValueError, match="CUDA"):
+            call()
+    with pytest.raises(ValueError, match="share a dtype"):
+        fa.fwd(q, q.float(), q, _BM())
+    with pytest.raises(ValueError, match="seg_ids"):
+        fa.block_mask("document", 1, 1, 4, 4, seg_ids=torch.zeros((1, 4), dtype=torch.int64))
+
+
+def test_block_mask_size_in_bytes(fa):
+    """fa_block_mask_size: nq, nkv and the bytes of each index array."""
+    lib = fa.load_library()
+    nq, nkv, nb = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_size_t()
+    assert lib.fa_block_mask_size(2, 3, 300, 129, ctypes.byref(nq), ctypes.byref(nkv), ctypes.byref(nb)) == fa.OK
+    assert (nq.value, nkv.value, nb.value) == (3, 2, 4 * 2 * 3 * 3 * 2)
+    assert lib.fa_block_mask_size(1, 1, 69632, 69632, None, None, ctypes.byref(nb)) == fa.OK
+    assert nb.value == 4 * 544 * 544
+    assert lib.fa_block_mask_size(1, 0, 1, 1, None, None, None) == fa.ERR_INVALID_ARG

@@ -110,7 +110,8 @@ def test_fp32_output():
 
 
 def test_matches_prefill_forward():
-    """The decoding and prefill paths agree on the same call (same BlockMask)."""
+    """The decoding and prefill paths agree on the same call (same BlockMask),
+    and each agrees with the fp64 oracle."""
     import torch
     from block_sparse_attention_fa_gb300 import fa
     w = _case("prefix_lm", "alibi", B=2, Hq=8, Hkv=2, q_len=4, kv_len=3000, prefix_len=1000)
@@ -122,6 +123,10 @@ def test_matches_prefill_forward():
     torch.cuda.synchronize()
     assert float((o1 - o2).abs().max()) < 1e-2
     assert float((l1 - l2).abs().max()) < 1e-3
+    o_ref, lse_ref = parity.run_oracle(w, q, k, v, None)
+    for o, lse, label in ((o1, l1, "decode"), (o2, l2, "prefill")):
+        parity.compare(o.double().cpu().numpy(), o_ref, lse.double().cpu().numpy(), lse_ref, "bf16",
+                       label=f"{label} vs oracle")
 
 
 def test_unsupported_shapes_are_errors():
