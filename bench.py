@@ -557,7 +557,7 @@ BACKWARD_WORKLOADS = ["causal_softcap_bf16", "window_alibi_softcap_bf16"]
 
 
 def backward_section(device, flush, steps, warmup, peaks, peak_src):
-    """Time fa_bwd (delta, dK/dV and dQ kernels, one CUDA graph replay, L2
+    """Time fa_bwd (row statistics, dK/dV and dQ kernels, one CUDA graph replay, L2
     flushed) after a forward on the same inputs.  Algorithmic FLOPs: 5
     products per visited tile (S, dP, dV, dK, dQ) = 2.5 x the forward's."""
     import torch
@@ -571,9 +571,10 @@ def backward_section(device, flush, steps, warmup, peaks, peak_src):
             device).to(torch.bfloat16)
         f32 = dict(dtype=torch.float32, device=device)
         dq, dk, dv = torch.empty(r.q.shape, **f32), torch.empty(r.k.shape, **f32), torch.empty(r.v.shape, **f32)
-        delta = torch.empty(lse.shape, **f32)
-        g = r.graph(lambda: fa.bwd(r.q, r.k, r.v, o, lse, dout, r.bm, dq=dq, dk=dk, dv=dv, delta=delta,
-                                   **r.score_kw))
+        rowstats = fa.bwd_rowstats(r.q)
+        r.bm.cols(workspace=r.ws)
+        g = r.graph(lambda: fa.bwd(r.q, r.k, r.v, o, lse, dout, r.bm, dq=dq, dk=dk, dv=dv, rowstats=rowstats,
+                                   workspace=r.ws, **r.score_kw))
         ms = statistics.mean(r.time_graph(g, steps, warmup, flush))
         flops = 2.5 * r.flops
         tf = flops / (ms * 1e-3) / 1e12
@@ -581,7 +582,7 @@ def backward_section(device, flush, steps, warmup, peaks, peak_src):
                      "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peaks["bf16_tflops"],
                                   "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4),
                                   "peak_source": peak_src, "algorithmic_flops": flops,
-                                  "kernels": ["bwd_delta_kernel", "bwd_dkdv_kernel", "bwd_dq_kernel"]}}
+                                  "kernels": ["bwd_rowstats_kernel", "bwd_tc_kernel<dK/dV>", "bwd_tc_kernel<dQ>"]}}
         del r, dq, dk, dv, dout
         torch.cuda.empty_cache()
     return out

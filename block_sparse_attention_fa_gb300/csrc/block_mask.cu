@@ -28,6 +28,9 @@
 //
 // One CTA per (q-block, mask head, mask batch) row of tiles; its threads take
 // consecutive kv blocks, so the index writes are ascending and coalesced.  The
+// transposed BlockMask the backward walks (the q-blocks that visit each kv
+// block, "q_indices" beside "kv_indices") comes from the same kernel with the
+// two axes exchanged.  The
 // partial and full lists are compacted with a warp ballot + block prefix sum.
 // For document masks the CTA also checks that its rows' ids are
 // non-decreasing and flags the workspace otherwise.
@@ -87,11 +90,15 @@ __device__ __forceinline__ TileClass classify_table(const MaskParams& m, const u
     return {any, all};
 }
 
+// COLS = false: one CTA per q-block (the BlockMask's rows of tiles), its
+// threads over the kv blocks.  COLS = true: the transposed BlockMask, one CTA
+// per kv block, its threads over the q-blocks that visit it; the same
+// classification of the same tiles, so the two are transposes of each other.
+template <bool COLS>
 __global__ void __launch_bounds__(kBuildThreads) block_mask_kernel(const BuildParams p) {
-    const int qb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int outer = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int n_outer = COLS ? p.nkv : p.nq, n_inner = COLS ? p.nq : p.nkv;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int r0 = qb * kBlock;
-    const int r1 = min(r0 + kBlock - 1, p.q_len - 1);
     const bool doc = p.mask.kind == FA_MASK_DOCUMENT;
     const int32_t* seg_row =
         doc ? p.mask.seg + (size_t)(p.mask.seg_batch == 1 ? 0 : b) * p.mask.seg_len : nullptr;
@@ -102,6 +109,7 @@ __global__ void __launch_bounds__(kBuildThreads) block_mask_kernel(const BuildPa
     // Document masks need sorted ids: each segment row is checked once, by the
     // CTAs of head 0 (and batch 0 when the row is shared), pairs (r, r + 1).
     if (doc && h == 0 && (p.mask.seg_batch != 1 || b == 0)) {
+        const int r0 = outer * kBlock;
         const int end = min(r0 + kBlock, p.mask.seg_len - 1);
         bool bad = false;
         for (int r = r0 + tid; r < end; r += kBuildThreads) bad |= seg_row[r] > seg_row[r + 1];
@@ -111,24 +119,29 @@ __global__ void __launch_bounds__(kBuildThreads) block_mask_kernel(const BuildPa
         }
     }
 
-    const size_t row = ((size_t)b * p.H + h) * p.nq + qb;
-    int32_t* part_out = p.kv_indices + row * p.nkv;
-    int32_t* full_out = p.full_kv_indices + row * p.nkv;
-    const bool q_complete = (r1 - r0) == kBlock - 1;
+    const size_t row = ((size_t)b * p.H + h) * n_outer + outer;
+    int32_t* part_out = p.kv_indices + row * n_inner;
+    int32_t* full_out = p.full_kv_indices + row * n_inner;
+    // the outer block's in-range extent (rows of a q-block, or columns of a kv block)
+    const int o0 = outer * kBlock;
+    const int o1 = min(o0 + kBlock - 1, (COLS ? p.kv_len : p.q_len) - 1);
+    const bool o_complete = (o1 - o0) == kBlock - 1;
 
     __shared__ int warp_part[kBuildThreads / 32];
     __shared__ int warp_full[kBuildThreads / 32];
     int base_part = 0, base_full = 0;
 
-    for (int kb0 = 0; kb0 < p.nkv; kb0 += kBuildThreads) {
+    for (int kb0 = 0; kb0 < n_inner; kb0 += kBuildThreads) {
         const int kb = kb0 + tid;
         bool part = false, full = false;
-        if (kb < p.nkv) {
-            const int c0 = kb * kBlock;
-            const int c1 = min(c0 + kBlock - 1, p.kv_len - 1);
+        if (kb < n_inner) {
+            const int i0 = kb * kBlock;
+            const int i1 = min(i0 + kBlock - 1, (COLS ? p.q_len : p.kv_len) - 1);
+            const int r0 = COLS ? i0 : o0, r1 = COLS ? i1 : o1;
+            const int c0 = COLS ? o0 : i0, c1 = COLS ? o1 : i1;
             const TileClass t = table ? classify_table(p.mask, tab, r0, r1, c0, c1)
                                       : classify(p.mask, seg_row, r0, r1, c0, c1);
-            const bool complete = q_complete && (c1 - c0) == kBlock - 1;
+            const bool complete = o_complete && (i1 - i0) == kBlock - 1;
             full = t.any && t.all && complete;
             part = t.any && !full;
         }
@@ -156,8 +169,8 @@ __global__ void __launch_bounds__(kBuildThreads) block_mask_kernel(const BuildPa
         base_full += tot_full;
         __syncthreads();
     }
-    for (int t = base_part + tid; t < p.nkv; t += kBuildThreads) part_out[t] = -1;
-    for (int t = base_full + tid; t < p.nkv; t += kBuildThreads) full_out[t] = -1;
+    for (int t = base_part + tid; t < n_inner; t += kBuildThreads) part_out[t] = -1;
+    for (int t = base_full + tid; t < n_inner; t += kBuildThreads) full_out[t] = -1;
     if (tid == 0) {
         p.kv_num_blocks[row] = base_part;
         p.full_kv_num_blocks[row] = base_full;
@@ -168,7 +181,13 @@ __global__ void __launch_bounds__(kBuildThreads) block_mask_kernel(const BuildPa
 
 cudaError_t launch_block_mask_build(const BuildParams& p, cudaStream_t s) {
     const dim3 grid(p.nq, p.H, p.B);
-    block_mask_kernel<<<grid, kBuildThreads, 0, s>>>(p);
+    block_mask_kernel<false><<<grid, kBuildThreads, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_block_mask_build_cols(const BuildParams& p, cudaStream_t s) {
+    const dim3 grid(p.nkv, p.H, p.B);
+    block_mask_kernel<true><<<grid, kBuildThreads, 0, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -426,7 +426,38 @@ fa_status fa_fwd_decode(const fa_fwd_args* a, const fa_block_mask* bm, const fa_
     return ok();
 }
 
-fa_status fa_bwd(const fa_bwd_args* a, const fa_block_mask* bm, const fa_score_desc* sc, void* stream) {
+size_t fa_bwd_rowstats_bytes(int32_t B, int32_t Hq, int32_t q_len) {
+    if (B < 1 || Hq < 1 || q_len < 1) return 0;
+    return (size_t)2 * B * Hq * ceil_div(q_len, fa::kBlock) * fa::kBlock * sizeof(float);
+}
+
+fa_status fa_block_mask_build_cols(const fa_block_mask* bm, const fa_block_mask_cols* cols, void* workspace,
+                                   void* stream) {
+    fa_status st = check_block_mask(bm);
+    if (st != FA_OK) return st;
+    if (!cols || !cols->q_num_blocks || !cols->q_indices || !cols->full_q_num_blocks || !cols->full_q_indices)
+        return fail(FA_ERR_INVALID_ARG, "transposed block mask buffers must be non-NULL");
+    if (!workspace) return fail(FA_ERR_INVALID_ARG, "workspace is NULL");
+    fa::BuildParams p{};
+    p.B = bm->B;
+    p.H = bm->H;
+    p.q_len = bm->q_len;
+    p.kv_len = bm->kv_len;
+    p.nq = bm->nq;
+    p.nkv = bm->nkv;
+    p.mask = mask_params(bm);
+    p.kv_num_blocks = cols->q_num_blocks;
+    p.kv_indices = cols->q_indices;
+    p.full_kv_num_blocks = cols->full_q_num_blocks;
+    p.full_kv_indices = cols->full_q_indices;
+    p.ws = static_cast<uint32_t*>(workspace);
+    cudaError_t e = fa::launch_block_mask_build_cols(p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "transposed block mask build launch");
+    return ok();
+}
+
+fa_status fa_bwd(const fa_bwd_args* a, const fa_block_mask* bm, const fa_block_mask_cols* cols,
+                 const fa_score_desc* sc, void* workspace, void* stream) {
     if (!a) return fail(FA_ERR_INVALID_ARG, "bwd args are NULL");
     if (a->B < 1 || a->Hq < 1 || a->Hkv < 1 || a->q_len < 1 || a->kv_len < 1)
         return fail(FA_ERR_INVALID_ARG, "extents must be >= 1 (B=%d Hq=%d Hkv=%d q_len=%d kv_len=%d)", a->B,
@@ -434,18 +465,19 @@ fa_status fa_bwd(const fa_bwd_args* a, const fa_block_mask* bm, const fa_score_d
     if (a->Hq % a->Hkv != 0)
         return fail(FA_ERR_INVALID_ARG, "Hq (%d) must be a multiple of Hkv (%d)", a->Hq, a->Hkv);
     if (a->D != 64 && a->D != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d not supported (64 or 128)", a->D);
-    if (!a->q || !a->k || !a->v || !a->o || !a->dout || !a->lse || !a->dq || !a->dk || !a->dv || !a->delta)
-        return fail(FA_ERR_INVALID_ARG, "q, k, v, o, dout, lse, dq, dk, dv and delta must be non-NULL");
+    if (!a->q || !a->k || !a->v || !a->o || !a->dout || !a->lse || !a->dq || !a->dk || !a->dv || !a->rowstats)
+        return fail(FA_ERR_INVALID_ARG, "q, k, v, o, dout, lse, dq, dk, dv and rowstats must be non-NULL");
     if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v) || !aligned16(a->o) || !aligned16(a->dout))
         return fail(FA_ERR_INVALID_ARG, "q, k, v, o and dout must be 16-byte aligned");
-    if ((reinterpret_cast<uintptr_t>(a->dq) | reinterpret_cast<uintptr_t>(a->dk) |
-         reinterpret_cast<uintptr_t>(a->dv)) & 7u)
-        return fail(FA_ERR_INVALID_ARG, "dq, dk and dv must be 8-byte aligned");
-    if ((reinterpret_cast<uintptr_t>(a->lse) | reinterpret_cast<uintptr_t>(a->delta)) & 3u)
-        return fail(FA_ERR_INVALID_ARG, "lse and delta must be 4-byte aligned");
+    if (!aligned16(a->dq) || !aligned16(a->dk) || !aligned16(a->dv) || !aligned16(a->rowstats))
+        return fail(FA_ERR_INVALID_ARG, "dq, dk, dv and rowstats must be 16-byte aligned");
+    if (reinterpret_cast<uintptr_t>(a->lse) & 3u) return fail(FA_ERR_INVALID_ARG, "lse must be 4-byte aligned");
     if (!(std::isfinite(a->scale))) return fail(FA_ERR_INVALID_ARG, "scale must be finite");
+    if (!workspace) return fail(FA_ERR_INVALID_ARG, "workspace is NULL");
     fa_status st = check_block_mask(bm);
     if (st != FA_OK) return st;
+    if (!cols || !cols->q_num_blocks || !cols->q_indices || !cols->full_q_num_blocks || !cols->full_q_indices)
+        return fail(FA_ERR_INVALID_ARG, "the transposed block mask (cols) and its buffers must be non-NULL");
     if (bm->q_len != a->q_len || bm->kv_len != a->kv_len)
         return fail(FA_ERR_INVALID_ARG, "block mask was built for (%d, %d), not (%d, %d)", bm->q_len, bm->kv_len,
                     a->q_len, a->kv_len);
@@ -457,7 +489,8 @@ fa_status fa_bwd(const fa_bwd_args* a, const fa_block_mask* bm, const fa_score_d
     if (bm->mask.kind == FA_MASK_TABLE && bm->mask.table_batch != 1 && bm->mask.table_batch != a->B)
         return fail(FA_ERR_INVALID_ARG, "table_batch must be 1 or B=%d", a->B);
     if ((long long)a->B * a->Hq > 65535) return fail(FA_ERR_UNSUPPORTED, "B x Hq must be <= 65535");
-    if ((long long)a->B * a->Hq * a->q_len > 2147483647LL)
+    if (bm->nq > 65535 || bm->nkv > 65535) return fail(FA_ERR_UNSUPPORTED, "at most 65535 blocks per sequence");
+    if ((long long)a->B * a->Hq * bm->nq * fa::kBlock > 1073741823LL)
         return fail(FA_ERR_UNSUPPORTED, "too many query rows");
     fa_score_desc score;
     if ((st = check_score(sc, &score)) != FA_OK) return st;
@@ -473,6 +506,7 @@ fa_status fa_bwd(const fa_bwd_args* a, const fa_block_mask* bm, const fa_score_d
     p.scale = a->scale > 0.f ? a->scale : 1.0f / std::sqrt((float)a->D);
     p.bm = {bm->B, bm->H, bm->nq, bm->nkv, bm->kv_num_blocks, bm->kv_indices, bm->full_kv_num_blocks,
             bm->full_kv_indices};
+    p.cols = {cols->q_num_blocks, cols->q_indices, cols->full_q_num_blocks, cols->full_q_indices};
     p.mask = mask_params(bm);
     p.score = {score.kind, score.softcap, score.alibi_slopes, score.rel_bias, score.rel_max};
     p.q = a->q;
@@ -481,11 +515,18 @@ fa_status fa_bwd(const fa_bwd_args* a, const fa_block_mask* bm, const fa_score_d
     p.o = a->o;
     p.dout = a->dout;
     p.lse = a->lse;
-    p.delta = a->delta;
+    p.rowstats = a->rowstats;
     p.dq = a->dq;
     p.dk = a->dk;
     p.dv = a->dv;
-    cudaError_t e = fa::launch_bwd_bf16(p, static_cast<cudaStream_t>(stream));
+    p.ws = static_cast<uint32_t*>(workspace);
+    p.timeout_ns = (uint64_t)(a->timeout_ms ? a->timeout_ms : 2000u) * 1000000ull;
+    alignas(64) CUtensorMap tq, tk, tv, tg;
+    if ((st = make_tmap(&tq, a->q, a->B, a->Hq, a->q_len, a->D)) != FA_OK) return st;
+    if ((st = make_tmap(&tk, a->k, a->B, a->Hkv, a->kv_len, a->D)) != FA_OK) return st;
+    if ((st = make_tmap(&tv, a->v, a->B, a->Hkv, a->kv_len, a->D)) != FA_OK) return st;
+    if ((st = make_tmap(&tg, a->dout, a->B, a->Hq, a->q_len, a->D)) != FA_OK) return st;
+    cudaError_t e = fa::launch_bwd_tc(p, tq, tk, tv, tg, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
     return ok();
 }

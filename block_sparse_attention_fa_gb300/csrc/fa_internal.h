@@ -22,6 +22,15 @@ struct BlockMaskView {
     const int32_t* full_kv_indices;
 };
 
+// The transposed BlockMask (the q-blocks that visit each kv block), as the
+// backward's dK/dV kernel walks it.
+struct BlockMaskColsView {
+    const int32_t* q_num_blocks;       // [B][H][nkv]
+    const int32_t* q_indices;          // [B][H][nkv][nq]
+    const int32_t* full_q_num_blocks;
+    const int32_t* full_q_indices;
+};
+
 // A built-in mask_mod as the kernels see it.
 struct MaskParams {
     int kind;                     // fa_mask_kind
@@ -94,10 +103,13 @@ struct BwdParams {
     const void* o;                // the forward's output (bf16)
     const void* dout;             // upstream gradient of O (bf16)
     const float* lse;             // the forward's logsumexp
-    float* delta;                 // scratch [B][Hq][q_len]: rowsum(dO * O)
+    float* rowstats;              // scratch [2][B][Hq][nq * 128]: rowsum(dO * O), then -lse log2(e)
     float* dq;
     float* dk;
     float* dv;
+    BlockMaskColsView cols;
+    uint32_t* ws;
+    uint64_t timeout_ns;
 };
 
 struct BuildParams {
@@ -124,7 +136,9 @@ cudaError_t launch_fwd_bf16(const FwdParams& p, const CUtensorMap& tq, const CUt
                             const CUtensorMap& tv, cudaStream_t s);
 cudaError_t launch_decode_bf16(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                                cudaStream_t s);
-cudaError_t launch_bwd_bf16(const BwdParams& p, cudaStream_t s);
+cudaError_t launch_block_mask_build_cols(const BuildParams& p, cudaStream_t s);
+cudaError_t launch_bwd_tc(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const CUtensorMap& tg, cudaStream_t s);
 int decode_max_splits();
 int decode_max_rows();
 

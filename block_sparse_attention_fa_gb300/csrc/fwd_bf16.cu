@@ -45,6 +45,7 @@
 #include <math_constants.h>
 
 #include "tanh_poly.h"
+#include "tanh2_poly.h"
 #include "fa_internal.h"
 #include "ptx.cuh"
 
@@ -143,6 +144,53 @@ __device__ __forceinline__ void exp_pair(float& p0, float& p1, float x0, float x
     ffma2(a0, a1, x0, x1, sc, sc, nm, nm);
     p0 = ex2_approx(a0);
     p1 = ex2_approx(a1);
+}
+
+// Soft-cap, one 64-column half: from the raw q.k x (masked elements -inf),
+// p = 2^(C log2(e) tanh(a x) - m) with the capped score formed inside the
+// argument, x Q(x^2) + nm (TIER 2 or 4: the folded polynomial of that degree,
+// coefficients k0..k4; TIER 0: the exact form), P packed to bf16 into TMEM
+// (its first 32 columns) and the row sums into rs.  PARTIAL: elements with
+// x = -inf give exactly 0.
+template <int TIER, bool PARTIAL>
+__device__ __forceinline__ void softcap_exp_half(const float (&x)[64], float nm, float k0, float k1, float k2,
+                                                 float k3, float k4, float cap_in, float cap_out, uint32_t tP,
+                                                 float (&rs)[4]) {
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const int col = 32 * c + 2 * e;
+            const float x0 = x[col], x1 = x[col + 1];
+            float a0, a1;
+            if (TIER == 0) {
+                a0 = softcap_exact(x0 * cap_in, cap_out) + nm;
+                a1 = softcap_exact(x1 * cap_in, cap_out) + nm;
+            } else {
+                float w0, w1, q0, q1;
+                fmul2(w0, w1, x0, x1, x0, x1);
+                if (TIER == 4) {
+                    ffma2(q0, q1, w0, w1, k4, k4, k3, k3);
+                    ffma2(q0, q1, q0, q1, w0, w1, k2, k2);
+                } else {
+                    ffma2(q0, q1, w0, w1, k2, k2, k1, k1);
+                }
+                if (TIER == 4) ffma2(q0, q1, q0, q1, w0, w1, k1, k1);
+                ffma2(q0, q1, q0, q1, w0, w1, k0, k0);
+                ffma2(a0, a1, x0, x1, q0, q1, nm, nm);
+            }
+            if (PARTIAL) {
+                a0 = x0 > -CUDART_INF_F ? a0 : -CUDART_INF_F;
+                a1 = x1 > -CUDART_INF_F ? a1 : -CUDART_INF_F;
+            }
+            const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+            const int a2 = (e & 1) * 2;
+            fadd2(rs[a2], rs[a2 + 1], rs[a2], rs[a2 + 1], p0, p1);
+            pk[e] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16_nowait(tP + 16u * c, pk);
+    }
 }
 
 template <int D>
@@ -394,6 +442,24 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 mbar_arrive(bar(B_UNIT_FULL + slot));
                 ++k;
                 if (u < 0) break;
+                // This unit's Q tiles and first K / V tiles go to L2 now: the
+                // loads below wait for the previous unit to release the Q
+                // buffers and ring stages, and then find them there instead
+                // of in HBM.
+                if (!seq.empty()) {
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        if (seq.row[t].empty()) continue;
+#pragma unroll
+                        for (int c = 0; c < D / 64; ++c) tma_prefetch_4d(&tmQ, c * 64, (2 * pu.pr + t) * kBlock, pu.hq, pu.b);
+                    }
+                    const int kb0 = max(seq.row[0].head(), seq.row[1].head());
+#pragma unroll
+                    for (int c = 0; c < D / 64; ++c) {
+                        tma_prefetch_4d(&tmK, c * 64, kb0 * kBlock, pu.hkv, pu.b);
+                        tma_prefetch_4d(&tmV, c * 64, kb0 * kBlock, pu.hkv, pu.b);
+                    }
+                }
                 // the Q tile of each query block that visits anything
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
@@ -636,7 +702,8 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const float sl2 = p.scale * kLog2e;
         const bool doc = p.mask.kind == FA_MASK_DOCUMENT;
         constexpr bool table = TABLE;
-        float cap_in = 0.f, cap_out = 0.f, s_lim = 0.f;
+        float cap_in = 0.f, cap_out = 0.f, s_lim = 0.f, s_lim2 = 0.f;
+        float tr0 = 0.f, tr1 = 0.f, tr2 = 0.f;
         float tq0 = 0.f, tq1 = 0.f, tq2 = 0.f, tq3 = 0.f, tq4 = 0.f;
         if (SCORE == FA_SCORE_SOFTCAP || SCORE == FA_SCORE_ALIBI_SOFTCAP) {
             // C log2(e) tanh(a s) = s Q(s^2), Q_k = C log2(e) a c_k a^(2k),
@@ -653,6 +720,10 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             tq3 = base * a2 * a2 * a2 * kTanhC3;
             tq4 = base * a2 * a2 * a2 * a2 * kTanhC4;
             s_lim = kTanhRange / cap_in;
+            tr0 = base * kTanh2C0;
+            tr1 = base * a2 * kTanh2C1;
+            tr2 = base * a2 * a2 * kTanh2C2;
+            s_lim2 = kTanh2Range / cap_in;
         }
         int* seg_tile = reinterpret_cast<int*>(smem + L::kSegTile) + t * 256;
         uint32_t k = 0, n = 0, uq = 0, doc_tiles = 0;
@@ -803,7 +874,25 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                                 x[e] = fmaf(-slope_l2, fabsf(di - static_cast<float>(e)), x[e] * sa);
                         }
                     }
-                    if (SCORE == FA_SCORE_SOFTCAP || SCORE == FA_SCORE_ALIBI_SOFTCAP) {
+                    // Soft-cap alone: the cap is monotonic, so the row max is
+                    // taken on the raw scores and capped once per row, and the
+                    // capped score of every element is formed inside the
+                    // exponent's argument (below).  Here only the polynomial's
+                    // tier is chosen, for the warp's 32 rows at once: degree 2
+                    // while every |a s| <= kTanh2Range, degree 4 while <=
+                    // kTanhRange, the exact form beyond (rare: large logits).
+                    int tier = 0;
+                    if (SCORE == FA_SCORE_SOFTCAP) {
+                        float am[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int e = 0; e < 64; e += 8) {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) am[q] = fmax3(am[q], fabsf(x[e + q]), fabsf(x[e + 4 + q]));
+                        }
+                        const float amax = fmax3(fmaxf(am[0], am[1]), am[2], am[3]);
+                        tier = !__any_sync(0xffffffffu, amax > s_lim2) ? 2 : !__any_sync(0xffffffffu, amax > s_lim) ? 4 : 0;
+                    }
+                    if (SCORE == FA_SCORE_ALIBI_SOFTCAP) {
                         // The polynomial holds while |s| <= s_lim.  One pass of
                         // |x| maxima decides, for the warp's 32 rows at once,
                         // between it and the exact form (rare for soft-cap
@@ -893,7 +982,19 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
                         for (int q = 0; q < 4; ++q) m4[q] = fmax3(m4[q], x[e + q], x[e + 4 + q]);
                     }
-                    const float mx = fmax3(fmaxf(m4[0], m4[1]), m4[2], m4[3]) * sc;
+                    float mx = fmax3(fmaxf(m4[0], m4[1]), m4[2], m4[3]) * sc;
+                    if (SCORE == FA_SCORE_SOFTCAP && mx > -CUDART_INF_F) {
+                        // the capped max, by the same tier as the elements
+                        if (tier == 2) {
+                            const float w = mx * mx;
+                            mx *= fmaf(fmaf(w, tr2, tr1), w, tr0);
+                        } else if (tier == 4) {
+                            const float w = mx * mx;
+                            mx *= fmaf(fmaf(fmaf(fmaf(w, tq4, tq3), w, tq2), w, tq1), w, tq0);
+                        } else {
+                            mx = softcap_exact(mx * cap_in, cap_out);
+                        }
+                    }
                     const float m_new = fmaxf(m_use, mx);
                     // O and l follow every increase of the max
                     const bool need = (j > 0 || h > 0) && m_new > m_use;
@@ -904,19 +1005,34 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
                     // P = 2^(x sc - m) -> bf16 pairs into TMEM over S_t,h
                     float rs[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const int col = 32 * c + 2 * e;
-                            float p0, p1;
-                            exp_pair(p0, p1, x[col], x[col + 1], sc, nm);
-                            const int a2 = (e & 1) * 2;
-                            fadd2(rs[a2], rs[a2 + 1], rs[a2], rs[a2 + 1], p0, p1);
-                            pk[e] = pack_bf16x2(p0, p1);
+                    if (SCORE == FA_SCORE_SOFTCAP) {
+                        // P = 2^(cap(x) - m): the capped score formed in the
+                        // exponent's argument; masked elements (x = -inf) give 0
+                        const uint32_t tPh = tSh + lane_off;
+                        if (tier == 2) {
+                            if (partial) softcap_exp_half<2, true>(x, nm, tr0, tr1, tr2, 0.f, 0.f, cap_in, cap_out, tPh, rs);
+                            else softcap_exp_half<2, false>(x, nm, tr0, tr1, tr2, 0.f, 0.f, cap_in, cap_out, tPh, rs);
+                        } else if (tier == 4) {
+                            if (partial) softcap_exp_half<4, true>(x, nm, tq0, tq1, tq2, tq3, tq4, cap_in, cap_out, tPh, rs);
+                            else softcap_exp_half<4, false>(x, nm, tq0, tq1, tq2, tq3, tq4, cap_in, cap_out, tPh, rs);
+                        } else {
+                            softcap_exp_half<0, true>(x, nm, 0.f, 0.f, 0.f, 0.f, 0.f, cap_in, cap_out, tPh, rs);
                         }
-                        tmem_st16_nowait(tSh + lane_off + 16u * c, pk);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) {
+                            uint32_t pk[16];
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                const int col = 32 * c + 2 * e;
+                                float p0, p1;
+                                exp_pair(p0, p1, x[col], x[col + 1], sc, nm);
+                                const int a2 = (e & 1) * 2;
+                                fadd2(rs[a2], rs[a2 + 1], rs[a2], rs[a2 + 1], p0, p1);
+                                pk[e] = pack_bf16x2(p0, p1);
+                            }
+                            tmem_st16_nowait(tSh + lane_off + 16u * c, pk);
+                        }
                     }
                     l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
 

@@ -26,7 +26,7 @@ BLOCK = 128
 
 SYMBOLS = ("fa_workspace_bytes", "fa_block_mask_shape", "fa_block_mask_size", "fa_block_mask_build", "fa_fwd",
            "fa_fwd_noalloc", "fa_fwd_decode", "fa_decode_partials_bytes", "fa_decode_splits", "fa_bwd",
-           "fa_workspace_check", "fa_last_error", "fa_version")
+           "fa_block_mask_build_cols", "fa_bwd_rowstats_bytes", "fa_workspace_check", "fa_last_error", "fa_version")
 
 
 class FAError(RuntimeError):
@@ -70,7 +70,13 @@ class BwdArgs(ctypes.Structure):
                 ("kv_len", ctypes.c_int32), ("D", ctypes.c_int32), ("scale", ctypes.c_float),
                 ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("o", ctypes.c_void_p),
                 ("dout", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("dq", ctypes.c_void_p),
-                ("dk", ctypes.c_void_p), ("dv", ctypes.c_void_p), ("delta", ctypes.c_void_p)]
+                ("dk", ctypes.c_void_p), ("dv", ctypes.c_void_p), ("rowstats", ctypes.c_void_p),
+                ("timeout_ms", ctypes.c_uint32)]
+
+
+class BlockMaskColsStruct(ctypes.Structure):
+    _fields_ = [("q_num_blocks", ctypes.c_void_p), ("q_indices", ctypes.c_void_p),
+                ("full_q_num_blocks", ctypes.c_void_p), ("full_q_indices", ctypes.c_void_p)]
 
 
 _lib = None
@@ -109,8 +115,14 @@ def load_library(path: str = LIB_PATH):
     h.fa_decode_partials_bytes.argtypes = [ctypes.POINTER(FwdArgs), ctypes.c_int32]
     h.fa_decode_splits.restype = ctypes.c_int32
     h.fa_decode_splits.argtypes = [ctypes.POINTER(FwdArgs), ctypes.POINTER(BlockMaskStruct)]
+    h.fa_block_mask_build_cols.restype = ctypes.c_int
+    h.fa_block_mask_build_cols.argtypes = [ctypes.POINTER(BlockMaskStruct), ctypes.POINTER(BlockMaskColsStruct),
+                                           ctypes.c_void_p, ctypes.c_void_p]
+    h.fa_bwd_rowstats_bytes.restype = ctypes.c_size_t
+    h.fa_bwd_rowstats_bytes.argtypes = [ctypes.c_int32] * 3
     h.fa_bwd.restype = ctypes.c_int
-    h.fa_bwd.argtypes = [ctypes.POINTER(BwdArgs), ctypes.POINTER(BlockMaskStruct), ctypes.POINTER(ScoreDesc),
+    h.fa_bwd.argtypes = [ctypes.POINTER(BwdArgs), ctypes.POINTER(BlockMaskStruct),
+                         ctypes.POINTER(BlockMaskColsStruct), ctypes.POINTER(ScoreDesc), ctypes.c_void_p,
                          ctypes.c_void_p]
     h.fa_workspace_check.restype = ctypes.c_int
     h.fa_workspace_check.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
@@ -212,6 +224,26 @@ class BlockMask:
         ws = workspace or default_workspace(self.kv_num_blocks.device, stream)
         _check(load_library().fa_block_mask_build(ctypes.byref(self.struct), ws.ptr, _stream_ptr(stream)))
         return self
+
+    def cols(self, stream=None, workspace: Optional["Workspace"] = None, rebuild: bool = False) -> dict:
+        """The transposed lists (fa_block_mask_build_cols: the q-blocks that
+        visit each kv block), built on first use and kept with the mask."""
+        if getattr(self, "_cols", None) is None or rebuild:
+            dev = self.kv_num_blocks.device
+            if getattr(self, "_cols", None) is None:
+                t = {"q_num_blocks": torch.empty((self.B, self.H, self.nkv), dtype=torch.int32, device=dev),
+                     "q_indices": torch.empty((self.B, self.H, self.nkv, self.nq), dtype=torch.int32, device=dev),
+                     "full_q_num_blocks": torch.empty((self.B, self.H, self.nkv), dtype=torch.int32, device=dev),
+                     "full_q_indices": torch.empty((self.B, self.H, self.nkv, self.nq), dtype=torch.int32,
+                                                   device=dev)}
+                cs = BlockMaskColsStruct()
+                for k, v in t.items():
+                    setattr(cs, k, v.data_ptr())
+                self._cols, self._cols_struct = t, cs
+            ws = workspace or default_workspace(dev, stream)
+            _check(load_library().fa_block_mask_build_cols(ctypes.byref(self.struct), ctypes.byref(self._cols_struct),
+                                                           ws.ptr, _stream_ptr(stream)))
+        return self._cols
 
     def visited_tiles(self) -> int:
         return int(self.kv_num_blocks.sum().item() + self.full_kv_num_blocks.sum().item())
@@ -438,13 +470,22 @@ def fwd_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, bm: BlockMask,
     return out, lse
 
 
+def bwd_rowstats(q: torch.Tensor) -> torch.Tensor:
+    """fp32 scratch for fa_bwd: fa_bwd_rowstats_bytes() bytes as a flat tensor."""
+    B, Hq, Tq, _ = q.shape
+    n = load_library().fa_bwd_rowstats_bytes(B, Hq, Tq) // 4
+    return torch.empty(n, dtype=torch.float32, device=q.device)
+
+
 def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse: torch.Tensor,
         dout: torch.Tensor, bm: BlockMask, *, score: str = "none", softcap: float = 0.0,
         alibi_slopes: Optional[torch.Tensor] = None, rel_bias: Optional[torch.Tensor] = None, rel_max: int = 0,
         scale: Optional[float] = None, dq: Optional[torch.Tensor] = None, dk: Optional[torch.Tensor] = None,
-        dv: Optional[torch.Tensor] = None, delta: Optional[torch.Tensor] = None, stream=None):
+        dv: Optional[torch.Tensor] = None, rowstats: Optional[torch.Tensor] = None,
+        workspace: Optional[Workspace] = None, stream=None, timeout_ms: int = 0):
     """Backward of fwd (fa_bwd) for bf16 q, k, v, the forward's bf16 o and
-    its lse, and the upstream gradient dout; returns fp32 (dq, dk, dv)."""
+    its lse, and the upstream gradient dout; returns fp32 (dq, dk, dv).  The
+    BlockMask's transposed lists are built on first use (BlockMask.cols)."""
     for t in (q, k, v, o, dout):
         if t.dtype != torch.bfloat16 or not (t.is_cuda and t.is_contiguous() and t.dim() == 4):
             raise ValueError("q, k, v, o and dout must be contiguous CUDA bf16 tensors [B, H, T, D]")
@@ -452,22 +493,35 @@ def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse:
     Hkv, Tkv = k.shape[1], k.shape[2]
     if tuple(o.shape) != tuple(q.shape) or tuple(dout.shape) != tuple(q.shape):
         raise ValueError("o and dout must have q's shape")
+    if tuple(k.shape) != tuple(v.shape) or k.shape[0] != B or k.shape[3] != D:
+        raise ValueError("k and v must be [B, Hkv, kv_len, D] with q's B and D")
     f32 = dict(dtype=torch.float32, device=q.device)
     dq = torch.empty((B, Hq, Tq, D), **f32) if dq is None else dq
     dk = torch.empty((B, Hkv, Tkv, D), **f32) if dk is None else dk
     dv = torch.empty((B, Hkv, Tkv, D), **f32) if dv is None else dv
-    delta = torch.empty((B, Hq, Tq), **f32) if delta is None else delta
+    rowstats = bwd_rowstats(q) if rowstats is None else rowstats
     for name, t, shape in (("lse", lse, (B, Hq, Tq)), ("dq", dq, (B, Hq, Tq, D)), ("dk", dk, (B, Hkv, Tkv, D)),
-                           ("dv", dv, (B, Hkv, Tkv, D)), ("delta", delta, (B, Hq, Tq))):
+                           ("dv", dv, (B, Hkv, Tkv, D))):
         if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous() or tuple(t.shape) != shape:
             raise ValueError(f"{name} must be a contiguous CUDA float32 tensor of shape {shape}")
+    need = load_library().fa_bwd_rowstats_bytes(B, Hq, Tq)
+    if rowstats.dtype != torch.float32 or not rowstats.is_cuda or not rowstats.is_contiguous() \
+            or rowstats.numel() * 4 < need:
+        raise ValueError(f"rowstats must be a contiguous CUDA float32 tensor of at least {need} bytes")
+    if bm.q_len != Tq or bm.kv_len != Tkv:
+        raise ValueError(f"the BlockMask was built for ({bm.q_len}, {bm.kv_len}), not ({Tq}, {Tkv})")
     a = BwdArgs()
     a.B, a.Hq, a.Hkv, a.q_len, a.kv_len, a.D = B, Hq, Hkv, Tq, Tkv, D
     a.scale = 0.0 if scale is None else float(scale)
     a.q, a.k, a.v, a.o, a.dout = q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr()
-    a.lse, a.dq, a.dk, a.dv, a.delta = lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), delta.data_ptr()
+    a.lse, a.dq, a.dk, a.dv = lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr()
+    a.rowstats = rowstats.data_ptr()
+    a.timeout_ms = timeout_ms
     sc = _score_desc(score, softcap, alibi_slopes, rel_bias, rel_max)
-    _check(load_library().fa_bwd(ctypes.byref(a), ctypes.byref(bm.struct), ctypes.byref(sc), _stream_ptr(stream)))
+    ws = workspace or default_workspace(q.device, stream)
+    bm.cols(stream=stream, workspace=ws)
+    _check(load_library().fa_bwd(ctypes.byref(a), ctypes.byref(bm.struct), ctypes.byref(bm._cols_struct),
+                                 ctypes.byref(sc), ws.ptr, _stream_ptr(stream)))
     return dq, dk, dv
 
 

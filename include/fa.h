@@ -271,6 +271,30 @@ size_t fa_decode_partials_bytes(const fa_fwd_args *a, int32_t num_splits);
  * be valid).                                                                */
 int32_t fa_decode_splits(const fa_fwd_args *a, const fa_block_mask *bm);
 
+/* The transposed BlockMask: for each kv block, the q-blocks whose BlockMask
+ * row lists it, split the same way into partial and full tiles (what
+ * FlexAttention's BlockMask keeps beside kv_indices for the backward:
+ * q_num_blocks / q_indices; FlexAttention Guide, "Systems Mechanics", item 1
+ * tile sparsity and item 2 automatic differentiation).  Extents are those of
+ * the fa_block_mask it belongs to (B, H, nq, nkv):
+ *   q_num_blocks[B][H][nkv]        number of PARTIAL tiles in each kv column
+ *   q_indices[B][H][nkv][nq]       their q-block indices, ascending, then -1
+ *   full_q_num_blocks[B][H][nkv]   number of FULL tiles
+ *   full_q_indices[B][H][nkv][nq]  their q-block indices, ascending, then -1
+ * Caller-owned device int32 buffers.                                        */
+typedef struct fa_block_mask_cols {
+    int32_t *q_num_blocks;
+    int32_t *q_indices;
+    int32_t *full_q_num_blocks;
+    int32_t *full_q_indices;
+} fa_block_mask_cols;
+
+/* Build the transposed lists of `bm` (same mask_mod, same tiles; bm's own
+ * arrays are not read, so the two builds may run in either order).  One
+ * launch, asynchronous on `stream`; `workspace` as for fa_block_mask_build. */
+fa_status fa_block_mask_build_cols(const fa_block_mask *bm, const fa_block_mask_cols *cols, void *workspace,
+                                   void *stream);
+
 /* Backward of fa_fwd: the gradients of a loss with respect to q, k and v,
  * given its gradient dO with respect to O (the backward the FlexAttention
  * Guide's "Implementation" script takes through autograd), for the same
@@ -278,18 +302,21 @@ int32_t fa_decode_splits(const fa_fwd_args *a, const fa_block_mask *bm);
  *     P = exp(S' - lse) (S' the forward's masked, score_mod'ed scores),
  *     dP = dO V^T, Delta_i = sum_d dO_id O_id, dS = P o (dP - Delta) o
  *     d score_mod / d s, dV = P^T dO, dK = scale dS^T Q, dQ = scale dS K.
- * Only the tiles the BlockMask lists are visited, and the mask is evaluated
- * on partial tiles only.
+ * Only the tiles the BlockMask lists are visited (dK and dV along `cols`, the
+ * transposed lists built by fa_block_mask_build_cols, dQ along bm's rows),
+ * and the mask is evaluated on partial tiles only.
  *   q, k, v   as for fa_fwd, bf16.
  *   o, lse    the forward's bf16 O (flags 0) and lse of the same call.
  *   dout      device bf16 [B][Hq][q_len][D].
  *   dq        device fp32 [B][Hq][q_len][D]; dk, dv device fp32
  *             [B][Hkv][kv_len][D] (summed over the query heads of each kv
  *             head).  All three are written in full.
- *   delta     device fp32 scratch [B][Hq][q_len].
- * bf16 tensors 16-byte aligned, dq, dk, dv 8-byte, lse and delta 4-byte.
- * Three kernel launches, asynchronous on `stream`; no device-side waits, so
- * no workspace.                                                             */
+ *   rowstats  device fp32 scratch of fa_bwd_rowstats_bytes() bytes: Delta and
+ *             -lse log2(e) of every query row, padded to whole q-blocks.
+ * bf16 tensors 16-byte aligned, dq, dk, dv 16-byte, lse 4-byte, rowstats
+ * 16-byte.  Three kernel launches (row statistics, dK/dV, dQ), asynchronous on
+ * `stream`; their pipeline waits are bounded and report through `workspace`
+ * (fa_workspace_check).                                                     */
 typedef struct fa_bwd_args {
     int32_t B, Hq, Hkv, q_len, kv_len, D;
     float scale;
@@ -302,10 +329,16 @@ typedef struct fa_bwd_args {
     float *dq;
     float *dk;
     float *dv;
-    float *delta;
+    float *rowstats;
+    uint32_t timeout_ms;
 } fa_bwd_args;
 
-fa_status fa_bwd(const fa_bwd_args *a, const fa_block_mask *bm, const fa_score_desc *sc, void *stream);
+/* Bytes of fa_bwd's rowstats scratch: 2 x B x Hq x ceil(q_len / 128) x 128
+ * fp32 (0 if an extent is < 1).                                             */
+size_t fa_bwd_rowstats_bytes(int32_t B, int32_t Hq, int32_t q_len);
+
+fa_status fa_bwd(const fa_bwd_args *a, const fa_block_mask *bm, const fa_block_mask_cols *cols,
+                 const fa_score_desc *sc, void *workspace, void *stream);
 
 /* Synchronise `stream`, then report and clear the device-side flags in
  * `workspace`: FA_OK, FA_ERR_TIMEOUT or FA_ERR_DEVICE_CHECK (details in

@@ -31,7 +31,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted([
-        "fa_block_mask_build", "fa_block_mask_shape", "fa_block_mask_size", "fa_bwd", "fa_decode_partials_bytes", "fa_decode_splits", "fa_fwd",
+        "fa_block_mask_build", "fa_block_mask_build_cols", "fa_block_mask_shape", "fa_block_mask_size", "fa_bwd",
+        "fa_bwd_rowstats_bytes", "fa_decode_partials_bytes", "fa_decode_splits", "fa_fwd",
         "fa_fwd_decode", "fa_fwd_noalloc", "fa_last_error", "fa_version", "fa_workspace_bytes",
         "fa_workspace_check"])
 
@@ -54,10 +55,12 @@ def test_struct_layout_matches_header(fa, tmp_path):
 #include "fa.h"
 #define F(T, m) printf(#T "." #m " %zu\n", offsetof(T, m));
 int main(void) {
-  printf("fa_mask_desc %zu\nfa_block_mask %zu\nfa_score_desc %zu\nfa_fwd_args %zu\nfa_bwd_args %zu\n",
+  printf("fa_mask_desc %zu\nfa_block_mask %zu\nfa_score_desc %zu\nfa_fwd_args %zu\nfa_bwd_args %zu\n"
+         "fa_block_mask_cols %zu\n",
          sizeof(fa_mask_desc), sizeof(fa_block_mask), sizeof(fa_score_desc), sizeof(fa_fwd_args),
-         sizeof(fa_bwd_args));
-  F(fa_bwd_args, scale) F(fa_bwd_args, q) F(fa_bwd_args, dout) F(fa_bwd_args, lse) F(fa_bwd_args, delta)
+         sizeof(fa_bwd_args), sizeof(fa_block_mask_cols));
+  F(fa_bwd_args, scale) F(fa_bwd_args, q) F(fa_bwd_args, dout) F(fa_bwd_args, lse) F(fa_bwd_args, rowstats)
+  F(fa_bwd_args, timeout_ms) F(fa_block_mask_cols, q_indices) F(fa_block_mask_cols, full_q_indices)
   F(fa_mask_desc, seg_ids) F(fa_mask_desc, table) F(fa_mask_desc, table_batch)
   F(fa_block_mask, kv_num_blocks) F(fa_block_mask, full_kv_indices)
   F(fa_block_mask, mask) F(fa_score_desc, alibi_slopes) F(fa_score_desc, rel_max)
@@ -75,8 +78,10 @@ int main(void) {
     assert got["fa_score_desc"] == ctypes.sizeof(fa.ScoreDesc)
     assert got["fa_fwd_args"] == ctypes.sizeof(fa.FwdArgs)
     assert got["fa_bwd_args"] == ctypes.sizeof(fa.BwdArgs)
+    assert got["fa_block_mask_cols"] == ctypes.sizeof(fa.BlockMaskColsStruct)
     pairs = {"fa_mask_desc": fa.MaskDesc, "fa_block_mask": fa.BlockMaskStruct,
-             "fa_score_desc": fa.ScoreDesc, "fa_fwd_args": fa.FwdArgs, "fa_bwd_args": fa.BwdArgs}
+             "fa_score_desc": fa.ScoreDesc, "fa_fwd_args": fa.FwdArgs, "fa_bwd_args": fa.BwdArgs,
+             "fa_block_mask_cols": fa.BlockMaskColsStruct}
     for key, off in got.items():
         if "." in key:
             t, m = key.split(".")
@@ -243,7 +248,7 @@ def test_decode_split_choice(fa):
 def _bwd_args(fa, **kw):
     a = fa.BwdArgs()
     a.B, a.Hq, a.Hkv, a.q_len, a.kv_len, a.D = 1, 4, 4, 256, 256, 128
-    a.q = a.k = a.v = a.o = a.dout = a.lse = a.dq = a.dk = a.dv = a.delta = FAKE
+    a.q = a.k = a.v = a.o = a.dout = a.lse = a.dq = a.dk = a.dv = a.rowstats = FAKE
     for k, v in kw.items():
         setattr(a, k, v)
     return a
@@ -254,16 +259,32 @@ def _bwd_args(fa, **kw):
     ({"Hkv": 3}, {}, "ERR_INVALID_ARG", b"multiple"),
     ({"dout": None}, {}, "ERR_INVALID_ARG", b"non-NULL"),
     ({"o": FAKE + 8}, {}, "ERR_INVALID_ARG", b"16-byte"),
-    ({"dk": FAKE + 4}, {}, "ERR_INVALID_ARG", b"8-byte"),
-    ({"delta": FAKE + 2}, {}, "ERR_INVALID_ARG", b"4-byte"),
+    ({"dk": FAKE + 4}, {}, "ERR_INVALID_ARG", b"16-byte"),
+    ({"rowstats": FAKE + 8}, {}, "ERR_INVALID_ARG", b"16-byte"),
+    ({"lse": FAKE + 2}, {}, "ERR_INVALID_ARG", b"4-byte"),
     ({"q_len": 300}, {}, "ERR_INVALID_ARG", b"built for"),
     ({}, {"H": 2}, "ERR_INVALID_ARG", b"block mask H"),
 ])
 def test_bwd_rejects(fa, kw, bmkw, status, text):
     lib = fa.load_library()
-    st = lib.fa_bwd(ctypes.byref(_bwd_args(fa, **kw)), ctypes.byref(_bm(fa, **bmkw)), None, None)
+    cols = fa.BlockMaskColsStruct(FAKE, FAKE, FAKE, FAKE)
+    st = lib.fa_bwd(ctypes.byref(_bwd_args(fa, **kw)), ctypes.byref(_bm(fa, **bmkw)), ctypes.byref(cols), None,
+                    ctypes.c_void_p(FAKE), None)
     assert st == getattr(fa, status), lib.fa_last_error()
     assert text in lib.fa_last_error()
+
+
+def test_bwd_needs_cols_and_workspace(fa):
+    lib = fa.load_library()
+    cols = fa.BlockMaskColsStruct(FAKE, FAKE, FAKE, FAKE)
+    st = lib.fa_bwd(ctypes.byref(_bwd_args(fa)), ctypes.byref(_bm(fa)), None, None, ctypes.c_void_p(FAKE), None)
+    assert st == fa.ERR_INVALID_ARG and b"transposed" in lib.fa_last_error()
+    st = lib.fa_bwd(ctypes.byref(_bwd_args(fa)), ctypes.byref(_bm(fa)), ctypes.byref(cols), None, None, None)
+    assert st == fa.ERR_INVALID_ARG and b"workspace" in lib.fa_last_error()
+    st = lib.fa_block_mask_build_cols(ctypes.byref(_bm(fa)), None, ctypes.c_void_p(FAKE), None)
+    assert st == fa.ERR_INVALID_ARG and b"transposed" in lib.fa_last_error()
+    assert lib.fa_bwd_rowstats_bytes(2, 3, 300) == 2 * 2 * 3 * 3 * 128 * 4
+    assert lib.fa_bwd_rowstats_bytes(0, 3, 300) == 0
 
 
 def test_binding_rejects_wrong_tensors_before_the_library(fa):

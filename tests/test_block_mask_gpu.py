@@ -1,5 +1,7 @@
 """GPU BlockMask builder vs the oracle's brute-force tile scan: bit-exact on
-every array (counts, ascending indices, -1 padding), through the C ABI."""
+every array (counts, ascending indices, -1 padding), through the C ABI; and
+the transposed lists (fa_block_mask_build_cols) bit-exact against a
+brute-force transpose of the oracle's lists."""
 import numpy as np
 import pytest
 
@@ -18,6 +20,38 @@ def fa():
     return fam
 
 
+def transpose_lists(want):
+    """The transposed BlockMask by brute force from the oracle's lists: for
+    each kv block, the q-blocks whose row lists it as partial / full,
+    ascending, -1 padded."""
+    B, H, nq, nkv = want["kv_indices"].shape
+    out = {"q_num_blocks": np.zeros((B, H, nkv), np.int32), "q_indices": np.full((B, H, nkv, nq), -1, np.int32),
+           "full_q_num_blocks": np.zeros((B, H, nkv), np.int32),
+           "full_q_indices": np.full((B, H, nkv, nq), -1, np.int32)}
+    for b in range(B):
+        for h in range(H):
+            for src_n, src_i, dst_n, dst_i in (("kv_num_blocks", "kv_indices", "q_num_blocks", "q_indices"),
+                                               ("full_kv_num_blocks", "full_kv_indices", "full_q_num_blocks",
+                                                "full_q_indices")):
+                cols = [[] for _ in range(nkv)]
+                for qb in range(nq):
+                    for kb in want[src_i][b, h, qb, :want[src_n][b, h, qb]]:
+                        cols[kb].append(qb)
+                for kb in range(nkv):
+                    out[dst_n][b, h, kb] = len(cols[kb])
+                    out[dst_i][b, h, kb, :len(cols[kb])] = cols[kb]
+    return out
+
+
+def _check_cols(fa, bm, want, label):
+    import torch
+    got = {k: v.cpu().numpy() for k, v in bm.cols().items()}
+    fa.default_workspace(torch.device("cuda")).check()
+    exp = transpose_lists(want)
+    for key in exp:
+        np.testing.assert_array_equal(got[key], exp[key], err_msg=f"{label} transposed {key}")
+
+
 def _build_both(fa, mask, B, H, q_len, kv_len, window=0, prefix_len=0, seg=None):
     import torch
     seg_t = torch.from_numpy(seg).cuda() if seg is not None else None
@@ -28,6 +62,7 @@ def _build_both(fa, mask, B, H, q_len, kv_len, window=0, prefix_len=0, seg=None)
                              prefix_len=prefix_len, seg=seg)
     for key in want:
         np.testing.assert_array_equal(got[key], want[key], err_msg=f"{mask} {key}")
+    _check_cols(fa, bm, want, mask)
     return got
 
 
@@ -116,3 +151,4 @@ def test_builder_tables(fa, name, table, H):
     want = oracle.block_mask(mask="table", B=Bt, H=H, q_len=q_len, kv_len=kv_len, table=table)
     for key in want:
         np.testing.assert_array_equal(got[key], want[key], err_msg=f"{name} {key}")
+    _check_cols(fa, bm, want, name)

@@ -53,3 +53,42 @@ def test_softcap_polynomial_as_the_kernel_folds_it():
         want = C * np.tanh(np.float64(scale) * s / C) * log2e
         nz = np.abs(want) > 0
         assert np.max(np.abs(x[nz] - want[nz]) / np.abs(want[nz])) < 2e-5
+
+
+def tanh2_header():
+    text = open(os.path.join(CSRC, "tanh2_poly.h")).read()
+    c = [float(v) for v in re.findall(r"kTanh2C\d = ([-0-9.e]+)f;", text)]
+    U = float(re.search(r"kTanh2Range = ([-0-9.e]+)f;", text).group(1))
+    return c, U
+
+
+def test_tanh2_header_matches_derivation():
+    g = _gen()
+    c, maxerr = g.tanh_coeffs(g.TANH2_DEGREE, g.TANH2_RANGE)
+    hc, U = tanh2_header()
+    assert U == g.TANH2_RANGE == 0.5
+    np.testing.assert_allclose(hc, np.float32(c), rtol=0, atol=1e-7)
+    assert maxerr < 3e-5
+
+
+def test_softcap_degree2_tier_as_the_kernel_folds_it():
+    """The degree-2 tier the forward uses where every |scale s / C| <= 1/2:
+    x Q(x^2) + nm with Q_k = C log2(e) a c_k a^(2k), evaluated in fp32 with
+    fused multiply-adds, stays within 5e-5 relative of C tanh(a x) log2(e);
+    the capped row max taken from the raw max equals the max of the capped
+    scores (the cap is increasing), so the largest element's argument is 0."""
+    hc, U = tanh2_header()
+    log2e = 1.4426950408889634
+    for C, scale in [(50.0, 128 ** -0.5), (20.0, 64 ** -0.5), (1.0, 1.0)]:
+        a = np.float32(scale / C)
+        Q = [np.float32(C * log2e * a * ck * float(a) ** (2 * k)) for k, ck in enumerate(hc)]
+        x = np.linspace(-U / a, U / a, 200001).astype(np.float32)
+        w = (x * x).astype(np.float32)
+        q = np.float32(np.float64(w) * np.float64(Q[2]) + np.float64(Q[1])).astype(np.float32)
+        q = np.float32(np.float64(q) * np.float64(w) + np.float64(Q[0])).astype(np.float32)
+        got = (np.float64(x) * np.float64(q))
+        want = C * np.tanh(np.float64(a) * x) * log2e
+        nz = np.abs(want) > 0
+        assert np.max(np.abs(got[nz] - want[nz]) / np.abs(want[nz])) < 5e-5
+        # monotonic: the capped value of the largest raw score is the largest capped value
+        assert np.all(np.diff(got) >= 0)
