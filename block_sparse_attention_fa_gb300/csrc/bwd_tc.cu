@@ -10,8 +10,8 @@
 //     dS = P o (dP - Delta) o d score_mod / d s,
 //     dV = P^T dO,   dK = scale dS^T Q,   dQ = scale dS K.
 // Three launches:
-//   bwd_rowstats_kernel  Delta and -lse log2(e) per query row, padded to
-//                        whole q-blocks (padding rows: Delta 0, -inf).
+//   bwd_rowstats_kernel  -Delta and -lse log2(e) per query row, padded to
+//                        whole q-blocks (padding rows: 0 and -inf).
 //   bwd_tc_kernel<DKDV>  one CTA per (b, kv head, kv block): K and V stay in
 //                        shared memory; the visits are the (query head of the
 //                        group, q-block) pairs of the TRANSPOSED BlockMask
@@ -28,12 +28,12 @@
 // S and dP are computed in both kernels so that no gradient needs atomics and
 // the result does not depend on the order of the visits.
 //
-// Roles (320 threads): warps 0-3 and 4-7 are the elementwise warpgroups of
-// halves 0 and 1 (thread r of a warpgroup owns TMEM lane r: a key row in the
-// dK/dV kernel, a query row in the dQ kernel); warp 8 loads with TMA; warp 9
-// issues the tcgen05 MMAs (one elected lane).  The two halves ping-pong: while
-// warpgroup h turns S_h, dP_h into P_h, dS_h, the tensor pipe runs the other
-// half's products.  TMEM (512 columns): S_h at 64 h, dP_h at 128 + 64 h,
+// Roles (320 threads): warps 0-3 and 4-7 are two elementwise warpgroups
+// (thread r of a warpgroup owns TMEM lane r: a key row in the dK/dV kernel, a
+// query row in the dQ kernel; warpgroup g takes columns 32 g .. 32 g + 31 of
+// each half); warp 8 loads with TMA; warp 9 issues the tcgen05 MMAs (one
+// elected lane).  The two halves ping-pong: while the warpgroups turn S_h, dP_h
+// into P_h, dS_h, the tensor pipe runs the other half's products.  TMEM (512 columns): S_h at 64 h, dP_h at 128 + 64 h,
 // accumulators at 256 (dV or dQ) and 256 + D (dK).  Every wait is bounded as in
 // the forward (ptx.cuh): on timeout the CTA flags the workspace, the roles
 // leave their loops, copies and products in flight are waited for (again with
@@ -44,6 +44,7 @@
 #include "fa_internal.h"
 #include "ptx.cuh"
 #include "tanh_poly.h"
+#include "tanh2_poly.h"
 
 namespace fa {
 namespace {
@@ -54,7 +55,7 @@ constexpr float kLog2eT = 1.4426950408889634f;
 enum Mode { DKDV = 0, DQ = 1 };
 
 // Barriers: resident tiles; per ring stage FULL and EMPTY; per half h the
-// S_h / dP_h products (SD) and the elementwise results (PDS, 4 warps);
+// S_h / dP_h products (SD) and the elementwise results (PDS, all 8 warps);
 // accumulation done; the MMA warp's drain.
 constexpr int kMaxSt = 4;
 enum TcBar {
@@ -143,15 +144,6 @@ __device__ __forceinline__ int total_visits(const BwdParams& p, int mode, int b,
     return n;
 }
 
-// tanh(u) by the minimax polynomial of tanh_poly.h (|u| <= kTanhRange).
-__device__ __forceinline__ float tanh_poly(float u) {
-    const float w = u * u;
-    float q = fmaf(w, kTanhC4, kTanhC3);
-    q = fmaf(q, w, kTanhC2);
-    q = fmaf(q, w, kTanhC1);
-    q = fmaf(q, w, kTanhC0);
-    return u * q;
-}
 // tanh(u) for any u: 1 - 2 / (e^(2u) + 1) with the sign of u.
 __device__ __forceinline__ float tanh_exact(float u) {
     const float e = ex2_approx(2.f * kLog2eT * fabsf(u));
@@ -160,51 +152,122 @@ __device__ __forceinline__ float tanh_exact(float u) {
     return copysignf(fmaf(-2.f, r, 1.f), u);
 }
 
-// The elementwise step of 32 consecutive columns of one row: from the raw
-// q.k values x[e] and dP values y[e], P (into x, as probabilities) and dS
-// (into y), both fp32.  qi(e), kj(e): the query and key index of column e.
-// nl(e), dl(e): -lse log2(e) and Delta of the query of column e.
-template <int SCORE, typename QI, typename KJ, typename NL, typename DL, typename VIS>
-__device__ __forceinline__ void elem32(const BwdParams& p, int hq, float (&x)[32], float (&y)[32], QI qi, KJ kj,
-                                       NL nl, DL dl, VIS vis) {
-    const float sl2 = p.scale * kLog2eT;
+// d = a * b and d = a + b on two lanes at once (one FMA-pipe instruction).
+__device__ __forceinline__ void fmul2b(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+    ffma2(d0, d1, a0, a1, b0, b1, -0.f, -0.f);
+}
+
+// Per-chunk constants of the score_mod.
+struct ElemConst {
+    float sl2;        // scale log2(e)
+    float ci;         // soft-cap: scale / C (ALiBi then soft-cap: 1 / C)
+    float cap_out;    // C log2(e)
+    float slope;      // ALiBi: the query head's slope (base 2 for ALiBi alone, natural for the composite)
+    // tanh(ci x) = x Q(x^2) with Q_k = ci^(2k+1) c_k: degree 4 for |ci x| <=
+    // kTanhRange, degree 2 for |ci x| <= kTanh2Range; xlim4, xlim2 the
+    // matching bounds on |x| (x the raw q.k for the soft-cap alone, the
+    // scaled and biased score for the composite)
+    float q0, q1, q2, q3, q4, r0, r1, r2, xlim4, xlim2;
+};
+
+// The elementwise step of 32 consecutive columns of one row.  In: x = raw
+// q.k, y = raw dP (fp32, from TMEM).  Out: x = P (probabilities, 0 where
+// masked), y = dS = P (dP - Delta) d score_mod / d s, or -dS for the
+// soft-cap score_mods (one operation fewer; kDsSign gives the sign, which
+// the epilogue's scale takes back).  nl[e], nd[e]: -lse log2(e) and -Delta of
+// the query of column e (per column in the dK/dV kernel, the row's own in the
+// dQ kernel); vmask: bit e = column e visible (all ones on full tiles).  For
+// the position-dependent score_mods: d0 = the column-0 index minus the row
+// index, so that i - j (query minus key) of column e is sgn (d0 + e): sgn = +1
+// in the dK/dV kernel (columns are queries), -1 in the dQ kernel (columns
+// are keys).
+template <int SCORE>
+struct DsSign {
+    static constexpr float kValue = (SCORE == FA_SCORE_SOFTCAP || SCORE == FA_SCORE_ALIBI_SOFTCAP) ? -1.f : 1.f;
+};
+
+template <int SCORE, bool PARTIAL>
+__device__ __forceinline__ void elem_chunk(const BwdParams& p, int hq, const ElemConst& k, float (&x)[32],
+                                           float (&y)[32], const float (&nl)[32], const float (&nd)[32],
+                                           uint32_t vmask, int d0, int sgn) {
     if (SCORE == FA_SCORE_SOFTCAP || SCORE == FA_SCORE_ALIBI_SOFTCAP) {
-        const float C = p.score.softcap, invC = 1.f / C, cap_out = C * kLog2eT;
-        float slope = 0.f;
-        if (SCORE == FA_SCORE_ALIBI_SOFTCAP) slope = __ldg(p.score.slopes + hq);
-        float u[32];
+        if (SCORE == FA_SCORE_ALIBI_SOFTCAP) {
+            // x <- scale s - slope |i - j| (natural units, before the cap)
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+                const float b0 = fabsf(static_cast<float>(d0 + e)), b1 = fabsf(static_cast<float>(d0 + e + 1));
+                float s0, s1;
+                fmul2b(s0, s1, x[e], x[e + 1], p.scale, p.scale);
+                ffma2(x[e], x[e + 1], b0, b1, -k.slope, -k.slope, s0, s1);
+            }
+        }
         float am = 0.f;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-            float s = x[e] * p.scale;
-            if (SCORE == FA_SCORE_ALIBI_SOFTCAP) s = fmaf(-slope, fabsf(static_cast<float>(qi(e) - kj(e))), s);
-            u[e] = s * invC;
-            am = fmaxf(am, fabsf(u[e]));
-        }
-        const bool poly = !__any_sync(0xffffffffu, am > kTanhRange);
+        for (int e = 0; e < 32; e += 2) am = fmax3(am, fabsf(x[e]), fabsf(x[e + 1]));
+        const int tier = !__any_sync(0xffffffffu, am > k.xlim2) ? 2 : !__any_sync(0xffffffffu, am > k.xlim4) ? 4 : 0;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-            const float t = poly ? tanh_poly(u[e]) : tanh_exact(u[e]);
-            const float pr = vis(e) ? ex2_approx(fmaf(t, cap_out, nl(e))) : 0.f;
-            x[e] = pr;
-            y[e] = pr * (y[e] - dl(e)) * fmaf(-t, t, 1.f);
+        for (int e = 0; e < 32; e += 2) {
+            float t0, t1;
+            if (tier == 2) {
+                float w0, w1, q0, q1;
+                fmul2b(w0, w1, x[e], x[e + 1], x[e], x[e + 1]);
+                ffma2(q0, q1, w0, w1, k.r2, k.r2, k.r1, k.r1);
+                ffma2(q0, q1, q0, q1, w0, w1, k.r0, k.r0);
+                fmul2b(t0, t1, x[e], x[e + 1], q0, q1);
+            } else if (tier == 4) {
+                float w0, w1, q0, q1;
+                fmul2b(w0, w1, x[e], x[e + 1], x[e], x[e + 1]);
+                ffma2(q0, q1, w0, w1, k.q4, k.q4, k.q3, k.q3);
+                ffma2(q0, q1, q0, q1, w0, w1, k.q2, k.q2);
+                ffma2(q0, q1, q0, q1, w0, w1, k.q1, k.q1);
+                ffma2(q0, q1, q0, q1, w0, w1, k.q0, k.q0);
+                fmul2b(t0, t1, x[e], x[e + 1], q0, q1);
+            } else {
+                t0 = tanh_exact(x[e] * k.ci);
+                t1 = tanh_exact(x[e + 1] * k.ci);
+            }
+            float a0, a1;
+            ffma2(a0, a1, t0, t1, k.cap_out, k.cap_out, nl[e], nl[e + 1]);
+            float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+            if (PARTIAL) {
+                p0 = (vmask >> e) & 1u ? p0 : 0.f;
+                p1 = (vmask >> (e + 1)) & 1u ? p1 : 0.f;
+            }
+            // -dS = P (dP - Delta) (t^2 - 1)
+            float m0, m1, dd0, dd1;
+            ffma2(m0, m1, t0, t1, t0, t1, -1.f, -1.f);
+            fadd2(dd0, dd1, y[e], y[e + 1], nd[e], nd[e + 1]);
+            fmul2b(dd0, dd1, dd0, dd1, p0, p1);
+            fmul2b(y[e], y[e + 1], dd0, dd1, m0, m1);
+            x[e] = p0;
+            x[e + 1] = p1;
         }
     } else {
-        float rb_base = 0.f;
-        (void)rb_base;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-            float a = fmaf(x[e], sl2, nl(e));
-            if (SCORE == FA_SCORE_ALIBI)
-                a = fmaf(-__ldg(p.score.slopes + hq) * kLog2eT, fabsf(static_cast<float>(qi(e) - kj(e))), a);
+        for (int e = 0; e < 32; e += 2) {
+            float a0, a1;
+            ffma2(a0, a1, x[e], x[e + 1], k.sl2, k.sl2, nl[e], nl[e + 1]);
+            if (SCORE == FA_SCORE_ALIBI) {
+                const float b0 = fabsf(static_cast<float>(d0 + e)), b1 = fabsf(static_cast<float>(d0 + e + 1));
+                ffma2(a0, a1, b0, b1, -k.slope, -k.slope, a0, a1);
+            }
             if (SCORE == FA_SCORE_REL_BIAS) {
                 const int R = p.score.rel_max;
-                const int rr = min(max(qi(e) - kj(e), -R), R);
-                a = fmaf(__ldg(p.score.rel_bias + (size_t)hq * (2 * R + 1) + rr + R), kLog2eT, a);
+                const float* rb = p.score.rel_bias + (size_t)hq * (2 * R + 1) + R;
+                a0 = fmaf(__ldg(rb + min(max(sgn * (d0 + e), -R), R)), kLog2eT, a0);
+                a1 = fmaf(__ldg(rb + min(max(sgn * (d0 + e + 1), -R), R)), kLog2eT, a1);
             }
-            const float pr = vis(e) ? ex2_approx(a) : 0.f;
-            x[e] = pr;
-            y[e] = pr * (y[e] - dl(e));
+            float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+            if (PARTIAL) {
+                p0 = (vmask >> e) & 1u ? p0 : 0.f;
+                p1 = (vmask >> (e + 1)) & 1u ? p1 : 0.f;
+            }
+            // dS = P (dP - Delta), with nd = -Delta
+            float dd0, dd1;
+            fadd2(dd0, dd1, y[e], y[e + 1], nd[e], nd[e + 1]);
+            fmul2b(y[e], y[e + 1], dd0, dd1, p0, p1);
+            x[e] = p0;
+            x[e + 1] = p1;
         }
     }
 }
@@ -229,33 +292,43 @@ __device__ __forceinline__ bool tc_visible(const BwdParams& p, int b, int i, int
     }
 }
 
-// The visible interval [lo, hi] of columns 0..31 of a chunk for the
-// closed-form masks (DOCUMENT and TABLE are tested per element instead).
-// dK/dV: the row is key j, columns are queries c0 + e; dQ: the row is query i,
-// columns are keys c0 + e.
+// The visible columns of a 32-column chunk of a partial tile, as a bit mask
+// (bit e: column e).  dK/dV: the row is key j, the columns queries c0 + e;
+// dQ: the row is query i, the columns keys c0 + e.  The closed-form masks
+// leave one interval per row; document and table masks are tested column by
+// column.  Bounds (i < q_len, j < kv_len) are part of the mask.
 template <int MODE>
-__device__ __forceinline__ void chunk_interval(const BwdParams& p, int row, int c0, int& lo, int& hi) {
+__device__ __forceinline__ uint32_t chunk_mask(const BwdParams& p, int b, int row, int c0) {
+    const int kind = p.mask.kind;
+    if (kind == FA_MASK_DOCUMENT || kind == FA_MASK_TABLE) {
+        uint32_t m = 0u;
+#pragma unroll 1
+        for (int e = 0; e < 32; ++e) {
+            const bool v = MODE == DKDV ? tc_visible(p, b, c0 + e, row) : tc_visible(p, b, row, c0 + e);
+            m |= (v ? 1u : 0u) << e;
+        }
+        return m;
+    }
+    int lo, hi;
     if (MODE == DKDV) {
         const int j = row;
         lo = 0;
         hi = p.q_len - 1 - c0;
-        switch (p.mask.kind) {
-            case FA_MASK_CAUSAL: lo = j - c0; break;
-            case FA_MASK_SLIDING_WINDOW: lo = j - c0; hi = min(hi, j + p.mask.window - c0); break;
-            case FA_MASK_PREFIX_LM: if (j >= p.mask.prefix_len) lo = j - c0; break;
-            default: break;
-        }
+        if (kind == FA_MASK_CAUSAL) lo = j - c0;
+        if (kind == FA_MASK_SLIDING_WINDOW) { lo = j - c0; hi = min(hi, j + p.mask.window - c0); }
+        if (kind == FA_MASK_PREFIX_LM && j >= p.mask.prefix_len) lo = j - c0;
     } else {
         const int i = row;
         lo = 0;
         hi = p.kv_len - 1 - c0;
-        switch (p.mask.kind) {
-            case FA_MASK_CAUSAL: hi = min(hi, i - c0); break;
-            case FA_MASK_SLIDING_WINDOW: hi = min(hi, i - c0); lo = i - p.mask.window - c0; break;
-            case FA_MASK_PREFIX_LM: hi = min(hi, max(i, p.mask.prefix_len - 1) - c0); break;
-            default: break;
-        }
+        if (kind == FA_MASK_CAUSAL) hi = min(hi, i - c0);
+        if (kind == FA_MASK_SLIDING_WINDOW) { hi = min(hi, i - c0); lo = i - p.mask.window - c0; }
+        if (kind == FA_MASK_PREFIX_LM) hi = min(hi, max(i, p.mask.prefix_len - 1) - c0);
     }
+    lo = max(lo, 0);
+    hi = min(hi, 31);
+    if (hi < lo) return 0u;
+    return (0xffffffffu >> (31 - hi)) & (0xffffffffu << lo);
 }
 
 __global__ void __launch_bounds__(256) bwd_rowstats_kernel(const BwdParams p) {
@@ -265,7 +338,7 @@ __global__ void __launch_bounds__(256) bwd_rowstats_kernel(const BwdParams p) {
     if (prow >= rows_pad) return;
     const long long bh = prow / ((long long)p.bm.nq * 128);
     const int i = static_cast<int>(prow - bh * p.bm.nq * 128);
-    float acc = 0.f, nl = -CUDART_INF_F;
+    float acc = 0.f, nl = -CUDART_INF_F;      // -Delta and -lse log2(e) of the row
     if (i < p.q_len) {
         const long long row = bh * p.q_len + i;
         const __nv_bfloat16* o = static_cast<const __nv_bfloat16*>(p.o) + row * p.D;
@@ -277,7 +350,7 @@ __global__ void __launch_bounds__(256) bwd_rowstats_kernel(const BwdParams p) {
 #pragma unroll
     for (int k = 16; k > 0; k >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, k);
     if (lane == 0) {
-        p.rowstats[prow] = acc;
+        p.rowstats[prow] = -acc;
         p.rowstats[rows_pad + prow] = nl;
     }
 }
@@ -316,7 +389,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const int n_visits = total_visits(p, MODE, b, hq0, heads, blk);
 
     if (threadIdx.x == 0) {
-        for (int k = 0; k < T_COUNT; ++k) mbar_init(bar(k), (k == T_PDS || k == T_PDS + 1) ? 4u : 1u);
+        for (int k = 0; k < T_COUNT; ++k) mbar_init(bar(k), (k == T_PDS || k == T_PDS + 1) ? 8u : 1u);
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -424,22 +497,28 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             mma_commit_elect(bar(T_SD + h));
         };
         // dK/dV: A1 += P_h S2_h (dV += P^T dO), A2 += dS_h S1_h (dK += dS^T Q);
-        // dQ: A1 += dS_h S1_h (dQ += dS K).  A from TMEM (bf16 in the first
-        // 32 columns of X1_h / X2_h), B the half's 64 rows MN-major, K = 64.
+        // dQ: A1 += dS_h S1_h (dQ += dS K).  A from TMEM (bf16: each 32-column
+        // chunk of X1_h / X2_h holds its 32 values in its first 16 columns),
+        // B the half's 64 rows MN-major, K = 64.
         auto issue_acc = [&](int h, int i, bool first) {
             const uint32_t st1 = sbase + L::kRing + (i % ST) * 2 * L::kTile, st2 = st1 + L::kTile;
             const uint64_t m1 = sdesc_sw128(st1 + 8192u * h, 16384, 1024), m2 = sdesc_sw128(st2 + 8192u * h, 16384, 1024);
+            // K step kk covers columns 16 kk .. 16 kk + 15 of the half, packed
+            // by chunk (kk >> 1) into its own first 16 TMEM columns
             if (MODE == DKDV) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_ts_elect(tA1, tX1 + 64u * h + kk * 8u, m2 + kk * 128u, idesc_a, (!first || kk > 0) ? 1u : 0u);
+                    mma_ts_elect(tA1, tX1 + 64u * h + 32u * (kk >> 1) + 8u * (kk & 1), m2 + kk * 128u, idesc_a,
+                                 (!first || kk > 0) ? 1u : 0u);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_ts_elect(tA2, tX2 + 64u * h + kk * 8u, m1 + kk * 128u, idesc_a, (!first || kk > 0) ? 1u : 0u);
+                    mma_ts_elect(tA2, tX2 + 64u * h + 32u * (kk >> 1) + 8u * (kk & 1), m1 + kk * 128u, idesc_a,
+                                 (!first || kk > 0) ? 1u : 0u);
             } else {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_ts_elect(tA1, tX2 + 64u * h + kk * 8u, m1 + kk * 128u, idesc_a, (!first || kk > 0) ? 1u : 0u);
+                    mma_ts_elect(tA1, tX2 + 64u * h + 32u * (kk >> 1) + 8u * (kk & 1), m1 + kk * 128u, idesc_a,
+                                 (!first || kk > 0) ? 1u : 0u);
             }
         };
         bool ok = n_visits > 0;
@@ -479,30 +558,72 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         const int row = blk * kBlock + r;            // key (dK/dV) or query (dQ) of this thread
         // dQ: the row's statistics, resident for every visit
-        float nl_row = 0.f, dl_row = 0.f;
+        float nl_row = 0.f, nd_row = 0.f;
         if (MODE == DQ) {
             const long long pr = ((long long)b * p.Hq + hq0) * p.bm.nq * 128 + row;
             nl_row = p.rowstats[rows_pad + pr];
-            dl_row = p.rowstats[pr];
+            nd_row = p.rowstats[pr];
+        }
+        ElemConst kc{};
+        kc.sl2 = p.scale * kLog2eT;
+        if (SCORE == FA_SCORE_SOFTCAP || SCORE == FA_SCORE_ALIBI_SOFTCAP) {
+            const float ci = (SCORE == FA_SCORE_SOFTCAP ? p.scale : 1.f) / p.score.softcap, c2 = ci * ci;
+            kc.ci = ci;
+            kc.cap_out = p.score.softcap * kLog2eT;
+            kc.q0 = ci * kTanhC0;
+            kc.q1 = ci * c2 * kTanhC1;
+            kc.q2 = ci * c2 * c2 * kTanhC2;
+            kc.q3 = ci * c2 * c2 * c2 * kTanhC3;
+            kc.q4 = ci * c2 * c2 * c2 * c2 * kTanhC4;
+            kc.r0 = ci * kTanh2C0;
+            kc.r1 = ci * c2 * kTanh2C1;
+            kc.r2 = ci * c2 * c2 * kTanh2C2;
+            kc.xlim4 = kTanhRange / ci;
+            kc.xlim2 = kTanh2Range / ci;
         }
         bool ok = true;
+        int cur_hq = -1;
         for (int i = 0; i < n_visits && ok; ++i) {
-            if (!mbar_wait_warp(bar(T_SD + h), i & 1, wc, TS_SD)) { ok = false; break; }
             const int s = i % ST;
-            if (!mbar_wait_warp(bar(T_FULL + s), (i / ST) & 1, wc, TS_FULL_E)) { ok = false; break; }
-            tc_fence_after();
-            const int other = info[4 * s + 0], hq = info[4 * s + 1];
-            const bool partial = info[4 * s + 2] != 0;
-            const float* sst = reinterpret_cast<const float*>(smem + L::kStats + s * 1024u);
+            // Both warpgroups work on the same half, warpgroup g on its chunk
+            // g (32 columns); while they turn to the other half, the tensor
+            // pipe runs this half's products and the next visit's S, dP.
 #pragma unroll 1
-            for (int c = 0; c < 2; ++c) {
-                const int cb = 64 * h + 32 * c;               // column of the chunk within the tile
+            for (int hh = 0; hh < 2; ++hh) {
+                if (!mbar_wait_warp(bar(T_SD + hh), i & 1, wc, TS_SD)) { ok = false; break; }
+                if (hh == 0 && !mbar_wait_warp(bar(T_FULL + s), (i / ST) & 1, wc, TS_FULL_E)) { ok = false; break; }
+                tc_fence_after();
+                const int other = info[4 * s + 0], hq = info[4 * s + 1];
+                const bool partial = info[4 * s + 2] != 0;
+                if ((SCORE == FA_SCORE_ALIBI || SCORE == FA_SCORE_ALIBI_SOFTCAP) && hq != cur_hq) {
+                    kc.slope = __ldg(p.score.slopes + hq) * (SCORE == FA_SCORE_ALIBI ? kLog2eT : 1.f);
+                    cur_hq = hq;
+                }
+                const float* sst = reinterpret_cast<const float*>(smem + L::kStats + s * 1024u);
+                const int cb = 64 * hh + 32 * h;              // column of the chunk within the tile
                 const int col0 = other * kBlock + cb;         // query (dK/dV) or key (dQ) index of column 0
-                float x[32], y[32];
+                float x[32], y[32], nl[32], nd[32];
                 {
                     uint32_t rx[32], ry[32];
                     tmem_ld32_async(tX1 + lane_off + cb, rx);
                     tmem_ld32_async(tX2 + lane_off + cb, ry);
+                    // the columns' statistics while the loads are in flight
+                    if (MODE == DKDV) {
+                        const float4* n4 = reinterpret_cast<const float4*>(sst + cb);
+                        const float4* d4 = reinterpret_cast<const float4*>(sst + 128 + cb);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const float4 a = n4[q], bb = d4[q];
+                            nl[4 * q] = a.x; nl[4 * q + 1] = a.y; nl[4 * q + 2] = a.z; nl[4 * q + 3] = a.w;
+                            nd[4 * q] = bb.x; nd[4 * q + 1] = bb.y; nd[4 * q + 2] = bb.z; nd[4 * q + 3] = bb.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            nl[e] = nl_row;
+                            nd[e] = nd_row;
+                        }
+                    }
                     tmem_wait_ld(rx);
                     tmem_wait_ld(ry);
 #pragma unroll
@@ -511,28 +632,13 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                         y[e] = __uint_as_float(ry[e]);
                     }
                 }
-                // the visible interval of the chunk (closed-form masks)
-                int lo = 0, hi = 31;
-                const bool per_elem = partial && (p.mask.kind == FA_MASK_DOCUMENT || p.mask.kind == FA_MASK_TABLE);
-                if (partial && !per_elem) chunk_interval<MODE>(p, row, col0, lo, hi);
-                auto vis = [&](int e) -> bool {
-                    if (!partial) return true;
-                    if (per_elem)
-                        return MODE == DKDV ? tc_visible(p, b, col0 + e, row) : tc_visible(p, b, row, col0 + e);
-                    return e >= lo && e <= hi;
-                };
-                if (MODE == DKDV) {
-                    auto qi = [&](int e) { return col0 + e; };
-                    auto kj = [&](int e) { return row; };
-                    auto nl = [&](int e) { return sst[cb + e]; };
-                    auto dl = [&](int e) { return sst[128 + cb + e]; };
-                    elem32<SCORE>(p, hq, x, y, qi, kj, nl, dl, vis);
+                // i - j of column e is sgn (d0 + e)
+                const int d0 = col0 - row, sgn = MODE == DKDV ? 1 : -1;
+                if (partial) {
+                    const uint32_t vmask = chunk_mask<MODE>(p, b, row, col0);
+                    elem_chunk<SCORE, true>(p, hq, kc, x, y, nl, nd, vmask, d0, sgn);
                 } else {
-                    auto qi = [&](int e) { return row; };
-                    auto kj = [&](int e) { return col0 + e; };
-                    auto nl = [&](int e) { return nl_row; };
-                    auto dl = [&](int e) { return dl_row; };
-                    elem32<SCORE>(p, hq, x, y, qi, kj, nl, dl, vis);
+                    elem_chunk<SCORE, false>(p, hq, kc, x, y, nl, nd, 0xffffffffu, d0, sgn);
                 }
                 uint32_t pk[16], dk[16];
 #pragma unroll
@@ -540,14 +646,15 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                     pk[e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
                     dk[e] = pack_bf16x2(y[2 * e], y[2 * e + 1]);
                 }
-                // P (dK/dV only) and dS over the columns already read
-                if (MODE == DKDV) tmem_st16_nowait(tX1 + lane_off + 64u * h + 16u * c, pk);
-                tmem_st16_nowait(tX2 + lane_off + 64u * h + 16u * c, dk);
+                // P (dK/dV only) and dS into the first 16 columns of the
+                // chunk's own 32 (read above by this warp only)
+                if (MODE == DKDV) tmem_st16_nowait(tX1 + lane_off + cb, pk);
+                tmem_st16_nowait(tX2 + lane_off + cb, dk);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(T_PDS + hh));
             }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(T_PDS + h));
         }
         // ---------------------------------------------------------- epilogue
         // dK/dV: warpgroup 0 writes dV (A1), warpgroup 1 dK (A2, times scale);
@@ -568,7 +675,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 tacc = h == 0 ? tA1 : tA2;
                 ncol = D;
                 col_base = 0;
-                mul = h == 0 ? 1.f : p.scale;
+                mul = h == 0 ? 1.f : DsSign<SCORE>::kValue * p.scale;   // the elementwise step keeps +-dS
                 out += (((size_t)b * p.Hkv + hk) * p.kv_len) * D;
                 nrows = p.kv_len;
             } else {
@@ -576,7 +683,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 tacc = tA1;
                 ncol = D / 2;
                 col_base = h * (D / 2);
-                mul = p.scale;
+                mul = DsSign<SCORE>::kValue * p.scale;                  // the elementwise step keeps +-dS
                 nrows = p.q_len;
             }
             // staging rows of this warp (the ring is idle: every product has
