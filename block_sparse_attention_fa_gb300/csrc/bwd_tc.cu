@@ -690,14 +690,27 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             // completed and every copy has landed)
             uint8_t* stage = smem + L::kRing + warp * 32 * L::kStageRow;
             const int rows_left = nrows - (blk * kBlock + wq * 32);
-            for (int c = 0; c < ncol / 32; ++c) {
-                uint32_t v[32];
-                if (n_visits > 0) {
-                    tmem_ld32(tacc + lane_off + col_base + 32u * c, v);
-                } else {
+            // the row's accumulator columns in one batch of loads and one wait
+            constexpr int kMaxChunks = D / 32;
+            uint32_t acc[kMaxChunks][32];
+            const int nch = ncol / 32;
+            if (n_visits > 0) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = 0u;
-                }
+                for (int c = 0; c < kMaxChunks; ++c)
+                    if (c < nch) tmem_ld32_async(tacc + lane_off + col_base + 32u * c, acc[c]);
+#pragma unroll
+                for (int c = 0; c < kMaxChunks; ++c)
+                    if (c < nch) tmem_wait_ld(acc[c]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < kMaxChunks; ++c)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) acc[c][e] = 0u;
+            }
+#pragma unroll
+            for (int c = 0; c < kMaxChunks; ++c) {
+                if (c >= nch) break;
+                const uint32_t (&v)[32] = acc[c];
                 __syncwarp();
 #pragma unroll
                 for (int q = 0; q < 8; ++q)

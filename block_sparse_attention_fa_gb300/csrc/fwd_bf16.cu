@@ -82,14 +82,13 @@ enum Bar {
     B_P_FULL = B_S_FULL + 4,                    // four (2 t + h): the 4 softmax warps of tile t
     B_O_DONE = B_P_FULL + 4,                    // two: MMA commit after a unit's last P_t V
     B_O_UPD = B_O_DONE + 2,                     // two: MMA commit after every P_t V
-    B_SEG = B_O_UPD + 2,                        // two: the 4 softmax warps of tile t, per document tile
-    B_UNIT_FULL = B_SEG + 2,                    // two slots
+    B_UNIT_FULL = B_O_UPD + 2,                  // two slots
     B_UNIT_EMPTY = B_UNIT_FULL + 2,             // two slots
     B_DRAIN = B_UNIT_EMPTY + 2,                 // two: one per MMA warp
     B_COUNT = B_DRAIN + 2
 };
 enum Site : uint32_t { S_Q = 1, S_Q_EMPTY, S_K_FULL, S_K_EMPTY, S_V_FULL, S_V_EMPTY, S_S_FULL,
-                       S_P_FULL, S_O_DONE, S_DRAIN, S_LOAD_DRAIN, S_SEG, S_UNIT_FULL, S_UNIT_EMPTY,
+                       S_P_FULL, S_O_DONE, S_DRAIN, S_LOAD_DRAIN, S_UNIT_FULL, S_UNIT_EMPTY,
                        S_O_UPD };
 constexpr uint32_t kUnitConsumers = 10;   // one lane of each MMA warp and of each softmax warp
 // A unit-queue slot: the unit (-1 = none left), whether its pair visits any
@@ -113,29 +112,40 @@ __device__ __forceinline__ float softcap_exact(float u, float cap_out) {
     return copysignf(cap_out * fmaf(-2.f, r, 1.f), u);
 }
 
-// In a non-decreasing array of 128 ids: below = #{a < key}, upto = #{a <= key}.
-// Two rounds of independent loads: the last id of each 16-id block says how
-// many whole blocks lie below the key, then the one block that holds the
-// boundary is counted (four 16-byte loads).
-__device__ __forceinline__ void seg_bounds(const int* a, int key, int& below, int& upto) {
-    int bl = 0, bu = 0;
+// The segment ids of kv tile kb that this lane holds for the warp: tile
+// columns 4 lane .. 4 lane + 3 (INT_MAX past kv_len or for no tile).
+__device__ __forceinline__ void load_tile_ids(const int32_t* seg_row, int kb, int kv_len, int lane, int (&ids)[4]) {
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        const int v = a[16 * q + 15];
-        bl += v < key;
-        bu += v <= key;
+    for (int s = 0; s < 4; ++s) {
+        const int j = kb * kBlock + 4 * lane + s;
+        ids[s] = (kb >= 0 && j < kv_len) ? __ldg(seg_row + j) : INT_MAX;
     }
-    const int4* blo = reinterpret_cast<const int4*>(a + 16 * min(bl, 7));
-    const int4* bup = reinterpret_cast<const int4*>(a + 16 * min(bu, 7));
-    int cl = 0, cu = 0;
+}
+
+// For this lane's key: below = #{tile ids < key}, upto = #{tile ids <= key},
+// the tile's 128 ids held 4 per lane (load_tile_ids).  The warp's keys (its
+// rows' ids) are non-decreasing in the lane, so the warp walks its few
+// distinct keys and counts each with ballots: no shared memory, no barrier
+// with the other warps.
+__device__ __forceinline__ void seg_bounds_warp(const int (&ids)[4], int key, int& below, int& upto) {
+    int kcur = __reduce_min_sync(0xffffffffu, key);
+    below = 0;
+    upto = 0;
+    for (;;) {
+        int lt = 0, le = 0;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const int4 vl = blo[q], vu = bup[q];
-        cl += (vl.x < key) + (vl.y < key) + (vl.z < key) + (vl.w < key);
-        cu += (vu.x <= key) + (vu.y <= key) + (vu.z <= key) + (vu.w <= key);
+        for (int s = 0; s < 4; ++s) {
+            lt += __popc(__ballot_sync(0xffffffffu, ids[s] < kcur));
+            le += __popc(__ballot_sync(0xffffffffu, ids[s] <= kcur));
+        }
+        if (key == kcur) {
+            below = lt;
+            upto = le;
+        }
+        const int nk = __reduce_min_sync(0xffffffffu, key > kcur ? key : INT_MAX);
+        if (nk == INT_MAX) break;
+        kcur = nk;
     }
-    below = bl < 8 ? 16 * bl + cl : 128;
-    upto = bu < 8 ? 16 * bu + cu : 128;
 }
 
 // One pair of probabilities: p = 2^(x * sc - m) on the MUFU ex2 unit.
@@ -205,11 +215,10 @@ struct Layout {
     static constexpr uint32_t kAbort = kTmemSlot + 4;
     static constexpr uint32_t kUnitQ = kAbort + 4;        // 2 slots x kUnitWords int32
     static constexpr uint32_t kStepFlags = kUnitQ + 2 * 4 * kUnitWords;  // kStages x uint32: flags of each stage's step
-    static constexpr uint32_t kSegTile = (kStepFlags + 4 * kMaxStages + 15) & ~15u;  // [2 tiles][2][128] int32
     // per softmax warp, 32 rows x 64 bytes of O (+16 bytes of padding per row,
     // so that row-wise writes and the 4-lanes-per-row reads hit distinct banks)
     static constexpr uint32_t kOStageRow = 80;
-    static constexpr uint32_t kOStage = kSegTile + 2 * 2 * 128 * 4;
+    static constexpr uint32_t kOStage = (kStepFlags + 4 * kMaxStages + 15) & ~15u;
     static constexpr uint32_t kUsed = kOStage + 8 * 32 * kOStageRow;
     static constexpr uint32_t kDynamic = kUsed + 1024;    // + 1 KB to align the base to 1024
     static_assert(kDynamic <= 227u * 1024u, "shared memory budget");
@@ -350,9 +359,14 @@ struct PairSeq {
     }
 };
 
-// TABLE: the mask is a lookup table (FA_MASK_TABLE).  A template parameter,
-// so that the other masks' code carries none of the table's loads.
-template <int D, int SCORE, bool TABLE>
+// MK: the family of the mask_mod, a template parameter so that each
+// family's kernel carries none of the others' code (the table's loads cost up
+// to 14 % on the document workload, the documents' id counting 10 % on
+// causal soft-cap, when compiled into the other kernels): the closed-form
+// interval masks (full, causal, window, prefix-LM), document masks, lookup
+// tables.
+enum MaskFamily { MK_INTERVAL = 0, MK_DOCUMENT = 1, MK_TABLE = 2 };
+template <int D, int SCORE, int MK>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -374,7 +388,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         for (int k = 0; k < B_COUNT; ++k) {
             uint32_t cnt = 1;
             // one arrival per softmax warp of the tile
-            if ((k >= B_P_FULL && k < B_P_FULL + 4) || k == B_SEG || k == B_SEG + 1) cnt = 4;
+            if (k >= B_P_FULL && k < B_P_FULL + 4) cnt = 4;
             if (k == B_UNIT_EMPTY || k == B_UNIT_EMPTY + 1) cnt = kUnitConsumers;
             // a stage is free once both MMA warps have released it
             if (k >= B_K_EMPTY && k < B_K_EMPTY + kMaxStages) cnt = 2;
@@ -700,8 +714,8 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const uint32_t tP = tS;
         const uint32_t tO = tmem + 256u + D * t;
         const float sl2 = p.scale * kLog2e;
-        const bool doc = p.mask.kind == FA_MASK_DOCUMENT;
-        constexpr bool table = TABLE;
+        constexpr bool doc = MK == MK_DOCUMENT;
+        constexpr bool table = MK == MK_TABLE;
         float cap_in = 0.f, cap_out = 0.f, s_lim = 0.f, s_lim2 = 0.f;
         float tr0 = 0.f, tr1 = 0.f, tr2 = 0.f;
         float tq0 = 0.f, tq1 = 0.f, tq2 = 0.f, tq3 = 0.f, tq4 = 0.f;
@@ -725,15 +739,15 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             tr2 = base * a2 * a2 * kTanh2C2;
             s_lim2 = kTanh2Range / cap_in;
         }
-        int* seg_tile = reinterpret_cast<int*>(smem + L::kSegTile) + t * 256;
-        uint32_t k = 0, n = 0, uq = 0, doc_tiles = 0;
+        uint32_t k = 0, n = 0, uq = 0;
         bool ok = true;
         // A unit as this warpgroup sees it.  The next unit is taken from the
         // queue before the current one's epilogue, so that its per-thread
         // loads (segment ids, slope) are in flight while the epilogue runs;
         // the BlockMask row itself comes from the queue slot.
         struct Cur {
-            int u, qb, i, my_seg, seg_next;
+            int u, qb, i, my_seg;
+            int seg4[4];
             float slope_l2;
             Pair pu;
             RowSeq rs;
@@ -757,9 +771,8 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const int32_t* seg_row =
                 doc ? p.mask.seg + (size_t)(p.mask.seg_batch == 1 ? 0 : c.pu.b) * p.mask.seg_len : nullptr;
             c.my_seg = (doc && c.i < p.q_len) ? __ldg(seg_row + c.i) : 0;
-            // this thread's segment id in the first partial tile
-            const int kp = c.rs.next_part();
-            c.seg_next = (doc && kp >= 0 && kp * kBlock + r < p.kv_len) ? __ldg(seg_row + kp * kBlock + r) : INT_MAX;
+            // this lane's 4 segment ids of the first partial tile
+            if (doc) load_tile_ids(seg_row, c.rs.next_part(), p.kv_len, lane, c.seg4);
             // the slope in the units the score has when the bias is added:
             // base 2 for ALiBi alone, natural (before the cap) for the composite
             c.slope_l2 = SCORE == FA_SCORE_ALIBI           ? __ldg(p.score.slopes + c.pu.hq) * kLog2e
@@ -777,7 +790,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const Pair pu = cur.pu;
             const int qb = cur.qb, i = cur.i, my_seg = cur.my_seg;
             RowSeq rs = cur.rs;
-            int seg_next = cur.seg_next;
+            int seg4[4] = {cur.seg4[0], cur.seg4[1], cur.seg4[2], cur.seg4[3]};
             const float slope_l2 = cur.slope_l2;
             const bool active = !rs.empty();
             const int32_t* seg_row =
@@ -800,26 +813,12 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 const int c0 = kb * kBlock;
                 int seg_lo = 0, seg_hi = -1;
                 if (partial && doc) {
-                    // the tile's segment ids into shared memory (one per
-                    // thread), then each row's visible columns by counting
-                    // the ids below and up to its own (seg_bounds).  B_SEG + t
-                    // counts the tile's 4 warps (each arrives once its 32 ids
-                    // are written); the buffer alternates, and a warp reaching
-                    // document tile d+2 has seen every warp arrive at d+1,
-                    // i.e. finish with d.
-                    const uint32_t ph = doc_tiles & 1;
-                    ++doc_tiles;
-                    int* buf = seg_tile + ph * 128;
-                    buf[r] = seg_next;
-                    __threadfence_block();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(B_SEG + t));
-                    const int kp = rs.next_part();
-                    seg_next = (kp >= 0 && kp * kBlock + r < p.kv_len) ? __ldg(seg_row + kp * kBlock + r) : INT_MAX;
-                    if (!mbar_wait_warp(bar(B_SEG + t), ph, wc, S_SEG)) { ok = false; break; }
+                    // each row's visible columns: the tile's ids below and up
+                    // to its own (loaded by this warp one partial tile ahead)
                     int upto;
-                    seg_bounds(buf, my_seg, seg_lo, upto);
+                    seg_bounds_warp(seg4, my_seg, seg_lo, upto);
                     seg_hi = upto - 1;
+                    load_tile_ids(seg_row, rs.next_part(), p.kv_len, lane, seg4);
                 }
                 // The tile's two 64-column halves, each in its own S buffer:
                 // while this warpgroup works on one, the tensor pipe fills
@@ -1094,31 +1093,32 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             uint8_t* stage = smem + L::kOStage + warp * 32 * L::kOStageRow;
             const size_t head_row0 = ((size_t)pu.b * p.Hq + pu.hq) * p.q_len;
             const int rows_left = p.q_len - (qb * kBlock + wq * 32);   // rows of this warp that exist
+            // The whole row of O comes out of TMEM in one batch of loads and
+            // one wait (a load per chunk with its own wait cost about 1000
+            // cycles each while the tensor pipe runs the other tile's work).
+            uint32_t o[D / 32][32];
+            if (active) {
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) tmem_ld32_async(tO + lane_off + 32u * c, o[c]);
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) tmem_wait_ld(o[c]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[c][e] = 0u;
+            }
             const int nchunk = out32 ? D / 16 : D / 32;
-#pragma unroll 1
+#pragma unroll
             for (int c = 0; c < nchunk; ++c) {
                 uint32_t w[16];
                 if (out32) {
-                    uint32_t o[16];
-                    if (active) {
-                        tmem_ld16(tO + lane_off + 16u * c, o);
-                    } else {
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) o[e] = 0u;
-                    }
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(__uint_as_float(o[e]) * inv);
+                    for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(__uint_as_float(o[c >> 1][16 * (c & 1) + e]) * inv);
                 } else {
-                    uint32_t o[32];
-                    if (active) {
-                        tmem_ld32(tO + lane_off + 32u * c, o);
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = 0u;
-                    }
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
-                        w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+                        w[e] = pack_bf16x2(__uint_as_float(o[c][2 * e]) * inv, __uint_as_float(o[c][2 * e + 1]) * inv);
                 }
                 __syncwarp();    // the previous chunk's reads of the staging rows are done
 #pragma unroll
@@ -1147,10 +1147,10 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     }
 }
 
-template <int D, int SCORE, bool TABLE>
+template <int D, int SCORE, int MK>
 cudaError_t launch_one(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, cudaStream_t s) {
-    auto kern = fwd_bf16_kernel<D, SCORE, TABLE>;
+    auto kern = fwd_bf16_kernel<D, SCORE, MK>;
     constexpr uint32_t smem = Layout<D>::kDynamic;
     static int configured_dev = -1;
     int dev = 0;
@@ -1176,22 +1176,26 @@ cudaError_t launch_one(const FwdParams& p, const CUtensorMap& tq, const CUtensor
     return cudaGetLastError();
 }
 
-template <int D, bool TABLE>
+template <int D, int MK>
 cudaError_t launch_dt(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                       const CUtensorMap& tv, cudaStream_t s) {
     switch (p.score.kind) {
-        case FA_SCORE_SOFTCAP: return launch_one<D, FA_SCORE_SOFTCAP, TABLE>(p, tq, tk, tv, s);
-        case FA_SCORE_ALIBI: return launch_one<D, FA_SCORE_ALIBI, TABLE>(p, tq, tk, tv, s);
-        case FA_SCORE_REL_BIAS: return launch_one<D, FA_SCORE_REL_BIAS, TABLE>(p, tq, tk, tv, s);
-        case FA_SCORE_ALIBI_SOFTCAP: return launch_one<D, FA_SCORE_ALIBI_SOFTCAP, TABLE>(p, tq, tk, tv, s);
-        default: return launch_one<D, FA_SCORE_NONE, TABLE>(p, tq, tk, tv, s);
+        case FA_SCORE_SOFTCAP: return launch_one<D, FA_SCORE_SOFTCAP, MK>(p, tq, tk, tv, s);
+        case FA_SCORE_ALIBI: return launch_one<D, FA_SCORE_ALIBI, MK>(p, tq, tk, tv, s);
+        case FA_SCORE_REL_BIAS: return launch_one<D, FA_SCORE_REL_BIAS, MK>(p, tq, tk, tv, s);
+        case FA_SCORE_ALIBI_SOFTCAP: return launch_one<D, FA_SCORE_ALIBI_SOFTCAP, MK>(p, tq, tk, tv, s);
+        default: return launch_one<D, FA_SCORE_NONE, MK>(p, tq, tk, tv, s);
     }
 }
 
 template <int D>
 cudaError_t launch_d(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                      const CUtensorMap& tv, cudaStream_t s) {
-    return p.mask.kind == FA_MASK_TABLE ? launch_dt<D, true>(p, tq, tk, tv, s) : launch_dt<D, false>(p, tq, tk, tv, s);
+    switch (p.mask.kind) {
+        case FA_MASK_TABLE: return launch_dt<D, MK_TABLE>(p, tq, tk, tv, s);
+        case FA_MASK_DOCUMENT: return launch_dt<D, MK_DOCUMENT>(p, tq, tk, tv, s);
+        default: return launch_dt<D, MK_INTERVAL>(p, tq, tk, tv, s);
+    }
 }
 
 }  // namespace
