@@ -71,6 +71,10 @@ constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kMaxStages = 4;
+// With bf16 output the running max is raised (and O, l rescaled) only when a
+// half's max exceeds it by more than this many base-2 units (P then stays
+// <= 2^8); with fp32 output it follows every increase.
+constexpr float kLazyMax = 8.f;
 
 // Barriers (mbarrier indices); B_X + t is the barrier of query tile t, B_X + s
 // that of ring stage s.
@@ -807,6 +811,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             // l, so the row's largest probability is exactly 1 and its bf16
             // rounding is exact); l: sum of the fp32 probabilities.
             float m_use = -CUDART_INF_F, l = 0.f;
+            const float lazy = (p.flags & FA_OUT_FP32) ? 0.f : kLazyMax;
             for (int j = 0; !rs.empty(); ++j, ++n) {
                 const int kb = rs.head();
                 const bool partial = rs.pop();
@@ -995,11 +1000,18 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         }
                     }
                     const float m_new = fmaxf(m_use, mx);
-                    // O and l follow every increase of the max
-                    const bool need = (j > 0 || h > 0) && m_new > m_use;
+                    // A lazy max (bf16 output): O and l follow the max only
+                    // when it grows by more than kLazyMax (base 2), so P may
+                    // reach 2^kLazyMax; the first half of a unit sets it.
+                    // O = (P V) / l then carries the bf16 rounding of the
+                    // largest P, at most 2^-9 max|V|, the size of the bf16
+                    // output's own rounding.  With fp32 output the max is
+                    // exact (lazy = 0): the largest P is 1 and rounds exactly.
+                    const bool first = j == 0 && h == 0;
+                    const bool need = !first && m_new > m_use + lazy;
                     const float alpha = need ? ex2_approx(m_use - m_new) : 1.f;
                     if (need) l *= alpha;
-                    m_use = m_new;
+                    if (first || need) m_use = m_new;
                     const float nm = m_use == -CUDART_INF_F ? 0.f : -m_use;
 
                     // P = 2^(x sc - m) -> bf16 pairs into TMEM over S_t,h

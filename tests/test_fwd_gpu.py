@@ -132,6 +132,7 @@ def test_causal_softcap_bf16_output_floor():
     o_ref, lse_ref = parity.run_oracle(w, q, k, v, None, rows=rows)
     got = o.reshape(-1, w.D)[rows]
     excess = np.abs(got - o_ref) - (parity.BF16_MAX_ABS + parity.bf16_output_floor(o_ref, got))
+    print(f"bf16-output soft-cap: max abs {np.abs(got - o_ref).max():.4e}, worst excess over the bound {excess.max():.4e}")
     assert excess.max() <= 0, f"bf16 output over the bound by {excess.max():.3e}"
     assert np.linalg.norm(got - o_ref) / np.linalg.norm(o_ref) <= parity.BF16_REL_L2
     np.testing.assert_allclose(lse.reshape(-1)[rows], lse_ref, atol=parity.LSE_TOL["bf16"])
