@@ -120,6 +120,7 @@ struct BuildParams {
     int32_t* full_kv_num_blocks;
     int32_t* full_kv_indices;
     uint32_t* ws;
+    int fast_rows;                // set by the launcher: rows built in shared memory, stored as int4
 };
 
 // Sets this thread's fa_last_error() message and returns `st`.
