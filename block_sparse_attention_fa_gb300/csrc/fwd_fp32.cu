@@ -11,8 +11,9 @@
 // thread owns every sixteenth float4 of the head dimension (conflict-free
 // shared loads) and the 16 partial dot products meet by xor-shuffles.  Eight
 // CTAs cover a q-block, so even a 136-token problem spreads over 64 CTAs.
-// K/V are staged through shared memory 32 rows at a time, every load of a
-// stage issued before the first is used.
+// K/V are staged through shared memory 32 rows at a time; the next chunk's
+// loads are in flight while the current one computes, and a chunk of a
+// partial tile that no row of the CTA can see is skipped whole.
 #include <math_constants.h>
 
 #include "fa_internal.h"
@@ -86,33 +87,75 @@ __global__ void __launch_bounds__(kThreads32) fwd_fp32_kernel(const FwdParams p)
 
     float m = -CUDART_INF_F, l = 0.f;
 
-    for (int j = 0; j < n; ++j) {
-        const bool partial = j < n_part;
-        const int kb = partial ? part_idx[j] : full_idx[j - n_part];
-        for (int sub = 0; sub < kBlock / kChunk; ++sub) {
-            const int cs = kb * kBlock + sub * kChunk;
-            if (cs >= p.kv_len) break;
-            __syncthreads();
-            {
-                constexpr int kPer = kChunk * NV / kThreads32;      // float4 of K (and of V) per thread
-                float4 kr[kPer], vr[kPer];
-#pragma unroll
-                for (int t = 0; t < kPer; ++t) {
-                    const int e = tid + t * kThreads32, rr = e / NV, cc = e % NV;
-                    const bool in = cs + rr < p.kv_len;
-                    kr[t] = in ? k4[(size_t)(cs + rr) * NV + cc] : make_float4(0.f, 0.f, 0.f, 0.f);
-                    vr[t] = in ? v4[(size_t)(cs + rr) * NV + cc] : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-#pragma unroll
-                for (int t = 0; t < kPer; ++t) {
-                    const int e = tid + t * kThreads32, rr = e / NV, cc = e % NV;
-                    ks[rr][cc] = kr[t];
-                    vs[rr][cc] = vr[t];
+    // The CTA's rows [cr0, cr1].  A 32-key chunk of a partial tile that no
+    // row of the CTA can see (after every row under a causal mask, outside
+    // every row's window, in other documents) is skipped whole: its scores
+    // would all be -inf.  The test is exact and uniform over the CTA.
+    const int cr0 = qb * kBlock + part * kRows, cr1 = min(cr0 + kRows - 1, p.q_len - 1);
+    const int seg_lo = doc ? seg_row[cr0] : 0, seg_hi = doc ? seg_row[cr1] : 0;
+    auto chunk_visible = [&](int cs) -> bool {
+        const int ce = min(cs + kChunk - 1, p.kv_len - 1);
+        switch (p.mask.kind) {
+            case FA_MASK_CAUSAL: return cs <= cr1;
+            case FA_MASK_SLIDING_WINDOW: return cs <= cr1 && ce >= cr0 - p.mask.window;
+            case FA_MASK_PREFIX_LM: return cs < p.mask.prefix_len || cs <= cr1;
+            case FA_MASK_DOCUMENT: return seg_row[cs] <= seg_hi && seg_row[ce] >= seg_lo;
+            default: return true;
+        }
+    };
+    // The visited chunks in order: tile j of the row's lists (partial, then
+    // full), 32-key chunk `sub` of it.  next_chunk() moves (j, sub) to the
+    // next chunk to compute and reports its first key and tile kind.
+    int j = 0, sub = 0;
+    auto next_chunk = [&](int& cs, bool& partial) -> bool {
+        for (; j < n; ++j, sub = 0) {
+            partial = j < n_part;
+            const int kb = partial ? part_idx[j] : full_idx[j - n_part];
+            for (; sub < kBlock / kChunk; ++sub) {
+                cs = kb * kBlock + sub * kChunk;
+                if (cs >= p.kv_len) break;
+                if (!partial || chunk_visible(cs)) {
+                    ++sub;
+                    return true;
                 }
             }
-            if (doc && tid < kChunk) segs[tid] = cs + tid < p.kv_len ? seg_row[cs + tid] : 0;
-            __syncthreads();
-
+        }
+        return false;
+    };
+    // K and V of a chunk, from global memory into registers (kPer float4 of
+    // each per thread); the next chunk's are loaded while this one computes
+    constexpr int kPer = kChunk * NV / kThreads32;
+    float4 kr[kPer], vr[kPer];
+    int seg_r = 0;
+    auto fetch = [&](int cs) {
+#pragma unroll
+        for (int t = 0; t < kPer; ++t) {
+            const int e = tid + t * kThreads32, rr = e / NV, cc = e % NV;
+            const bool in = cs + rr < p.kv_len;
+            kr[t] = in ? k4[(size_t)(cs + rr) * NV + cc] : make_float4(0.f, 0.f, 0.f, 0.f);
+            vr[t] = in ? v4[(size_t)(cs + rr) * NV + cc] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        if (doc && tid < kChunk) seg_r = cs + tid < p.kv_len ? seg_row[cs + tid] : 0;
+    };
+    int cs_next;
+    bool part_next;
+    bool have = next_chunk(cs_next, part_next);
+    if (have) fetch(cs_next);
+    while (have) {
+        const int cs = cs_next;
+        const bool partial = part_next;
+        __syncthreads();                         // the previous chunk's reads of ks, vs are done
+#pragma unroll
+        for (int t = 0; t < kPer; ++t) {
+            const int e = tid + t * kThreads32, rr = e / NV, cc = e % NV;
+            ks[rr][cc] = kr[t];
+            vs[rr][cc] = vr[t];
+        }
+        if (doc && tid < kChunk) segs[tid] = seg_r;
+        __syncthreads();
+        have = next_chunk(cs_next, part_next);
+        if (have) fetch(cs_next);
+        {
             float s[kChunk];
             float mx = -CUDART_INF_F;
 #pragma unroll
