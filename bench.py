@@ -307,7 +307,7 @@ class Runner:
         return sec, h2d, d2h
 
 
-KERNEL_SOURCES = ["fwd_bf16.cu", "fa_api.cu", "ptx.cuh", "fa_internal.h", "tanh_poly.h"]
+KERNEL_SOURCES = ["fwd_bf16.cu", "fa_api.cu", "ptx.cuh", "fa_internal.h", "tanh_poly.h", "tanh2_poly.h"]
 
 
 def kernel_source_digest():
@@ -707,6 +707,10 @@ def main():
     ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--decode-only", action="store_true",
                     help="time only the split-KV decoding workloads and print their section")
+    ap.add_argument("--backward-only", action="store_true",
+                    help="time only the backward workloads and print their section")
+    ap.add_argument("--build-only", action="store_true",
+                    help="time only the BlockMask builder at scale and print its section")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -727,10 +731,15 @@ def main():
     from block_sparse_attention_fa_gb300 import fa
     fa.load_library()
 
-    if args.decode_only:
+    if args.decode_only or args.backward_only or args.build_only:
         flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
-        print(json.dumps({"decode": decode_section(device, flush, args.steps, args.warmup, peaks, peak_src)}),
-              flush=True)
+        if args.decode_only:
+            out = {"decode": decode_section(device, flush, args.steps, args.warmup, peaks, peak_src)}
+        elif args.backward_only:
+            out = {"backward": backward_section(device, flush, args.steps, args.warmup, peaks, peak_src)}
+        else:
+            out = {"build_at_scale": build_scale_section(device, flush, args.steps, args.warmup, peaks, peak_src)}
+        print(json.dumps(out), flush=True)
         return
 
     r = Runner(w, device)

@@ -38,6 +38,8 @@
 // the forward (ptx.cuh): on timeout the CTA flags the workspace, the roles
 // leave their loops, copies and products in flight are waited for (again with
 // a limit), TMEM is freed and the kernel returns.
+#include <algorithm>
+
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
@@ -59,14 +61,20 @@ enum Mode { DKDV = 0, DQ = 1 };
 // accumulation done; the MMA warp's drain.
 constexpr int kMaxSt = 4;
 enum TcBar {
-    T_R_FULL = 0,
-    T_FULL = 1, T_EMPTY = T_FULL + kMaxSt,
+    T_R_FULL = 0, T_R_EMPTY = 1,
+    T_FULL = 2, T_EMPTY = T_FULL + kMaxSt,
     T_SD = T_EMPTY + kMaxSt, T_PDS = T_SD + 2,
-    T_ACC = T_PDS + 2, T_DRAIN = T_ACC + 1,
+    T_ACC = T_PDS + 2, T_ACC_FREE = T_ACC + 1,
+    T_UNIT_FULL = T_ACC_FREE + 1, T_UNIT_EMPTY = T_UNIT_FULL + 2,
+    T_DRAIN = T_UNIT_EMPTY + 2,
     T_COUNT = T_DRAIN + 1
 };
 enum TcSite : uint32_t { TS_R = 101, TS_FULL, TS_EMPTY, TS_SD, TS_PDS, TS_ACC, TS_DRAIN, TS_LOAD_DRAIN,
-                         TS_FULL_E };
+                         TS_FULL_E, TS_R_EMPTY, TS_ACC_FREE, TS_UNIT_FULL, TS_UNIT_EMPTY };
+// A unit-queue slot: the unit (-1: none left), its visit count, b, first
+// query head, kv head, resident block.
+enum TcUnitWord { TU_UNIT = 0, TU_N, TU_B, TU_HQ0, TU_HK, TU_BLK, TU_WORDS = 8 };
+constexpr uint32_t kTcUnitConsumers = 9;    // the MMA warp and the 8 elementwise warps
 
 template <int D>
 struct TcLayout {
@@ -76,15 +84,16 @@ struct TcLayout {
     static constexpr uint32_t kRing = 2 * kTile;                 // per stage: streamed tiles 1 and 2
     static constexpr uint32_t kStats = kRing + kStages * 2 * kTile;   // per stage: -lse log2 e [128], Delta [128]
     static constexpr uint32_t kInfo = kStats + kStages * 1024;        // per stage: block, head, partial
-    static constexpr uint32_t kBars = kInfo + kStages * 16;
+    // epilogue staging: per warp 32 rows x 16 fp32, rows padded to 80 bytes
+    // (its own space: the ring is already taking the next unit's tiles)
+    static constexpr uint32_t kStageRow = 80;
+    static constexpr uint32_t kStage = kInfo + kStages * 16;
+    static constexpr uint32_t kUnitQ = kStage + 8 * 32 * kStageRow;   // 2 slots x TU_WORDS int32
+    static constexpr uint32_t kBars = kUnitQ + 2 * 4 * TU_WORDS;
     static constexpr uint32_t kTmemSlot = kBars + 8 * T_COUNT;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
     static constexpr uint32_t kUsed = kAbort + 12;
     static constexpr uint32_t kDynamic = kUsed + 1024;          // + 1 KB to align the base to 1024
-    // epilogue staging (after the last product): per warp 32 rows x 32 fp32,
-    // rows padded to 144 bytes, in the ring
-    static constexpr uint32_t kStageRow = 144;
-    static_assert(8 * 32 * kStageRow <= kStages * 2 * kTile, "epilogue staging fits in the ring");
     static_assert(kDynamic <= 227u * 1024u, "shared memory budget");
     static_assert(kStages <= kMaxSt, "too many stages");
 };
@@ -355,10 +364,44 @@ __global__ void __launch_bounds__(256) bwd_rowstats_kernel(const BwdParams p) {
     }
 }
 
+// The resident block of work unit u: dK/dV: kv block `blk` of (b, kv head
+// hk), lowest kv blocks first; dQ: q-block `blk` of (b, query head hq0),
+// highest q-blocks first.  Under causal masks both orders start with the
+// blocks that have the most visits.
+struct TcUnit {
+    int b, hq0, hk, heads, blk;
+};
+__device__ __forceinline__ TcUnit tc_decode_unit(const BwdParams& p, int mode, int u) {
+    TcUnit x;
+    if (mode == DKDV) {
+        const int bh = u % (p.B * p.Hkv);
+        x.blk = u / (p.B * p.Hkv);
+        x.b = bh / p.Hkv;
+        x.hk = bh % p.Hkv;
+        x.hq0 = x.hk * p.group;
+        x.heads = p.group;
+    } else {
+        const int bh = u % (p.B * p.Hq);
+        x.blk = p.bm.nq - 1 - u / (p.B * p.Hq);
+        x.b = bh / p.Hq;
+        x.hq0 = bh % p.Hq;
+        x.hk = x.hq0 / p.group;
+        x.heads = 1;
+    }
+    return x;
+}
+
+// Persistent: one CTA per SM takes units from a counter in the workspace and
+// passes each through a two-slot queue in shared memory.  While the
+// elementwise warps write a unit's gradients out, the loader already fetches
+// the next unit's resident tiles (after the last product that reads them,
+// R_EMPTY) and the MMA warp starts its S, dP (its accumulations wait for
+// ACC_FREE, the epilogue's read of the accumulators).
 template <int D, int SCORE, int MODE>
 __global__ void __launch_bounds__(kTcThreads, 1)
 bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG, const BwdParams p) {
+              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG, const BwdParams p,
+              int num_units) {
     using L = TcLayout<D>;
     constexpr int ST = L::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -369,27 +412,16 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + L::kTmemSlot);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
     volatile int* info = reinterpret_cast<volatile int*>(smem + L::kInfo);
+    volatile int* unit_q = reinterpret_cast<volatile int*>(smem + L::kUnitQ);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // The CTA's resident block: dK/dV: kv block `blk` of (b, kv head hk);
-    // dQ: q-block `blk` of (b, query head hq).
-    const int bh = blockIdx.x, blk = blockIdx.y;
-    int b, hq0, hk, heads;
-    if (MODE == DKDV) {
-        b = bh / p.Hkv;
-        hk = bh % p.Hkv;
-        hq0 = hk * p.group;
-        heads = p.group;
-    } else {
-        b = bh / p.Hq;
-        hq0 = bh % p.Hq;
-        hk = hq0 / p.group;
-        heads = 1;
-    }
-    const int n_visits = total_visits(p, MODE, b, hq0, heads, blk);
-
     if (threadIdx.x == 0) {
-        for (int k = 0; k < T_COUNT; ++k) mbar_init(bar(k), (k == T_PDS || k == T_PDS + 1) ? 8u : 1u);
+        for (int k = 0; k < T_COUNT; ++k) {
+            uint32_t cnt = 1;
+            if (k == T_PDS || k == T_PDS + 1 || k == T_ACC_FREE) cnt = 8;
+            if (k == T_UNIT_EMPTY || k == T_UNIT_EMPTY + 1) cnt = kTcUnitConsumers;
+            mbar_init(bar(k), cnt);
+        }
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -412,62 +444,87 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
             tma_prefetch_desc(&tmG);
-            int last = -1;
-            bool r_loaded = false;
-            if (n_visits > 0) {
+            int last = -1, rr = 0;
+            uint32_t k = 0;
+            int i = 0;
+            bool ok = true;
+            while (ok) {
+                const uint32_t slot = k & 1;
+                if (k >= 2 && !mbar_wait(bar(T_UNIT_EMPTY + slot), ((k >> 1) - 1) & 1, wc, TS_UNIT_EMPTY)) break;
+                int u = static_cast<int>(atomicAdd(p.ws + WS_SCHED_NEXT, 1u));
+                if (u >= num_units) u = -1;
+                TcUnit un{};
+                int n = 0;
+                if (u >= 0) {
+                    un = tc_decode_unit(p, MODE, u);
+                    n = total_visits(p, MODE, un.b, un.hq0, un.heads, un.blk);
+                }
+                volatile int* qs = unit_q + TU_WORDS * slot;
+                qs[TU_UNIT] = u;
+                qs[TU_N] = n;
+                qs[TU_B] = un.b;
+                qs[TU_HQ0] = un.hq0;
+                qs[TU_HK] = un.hk;
+                qs[TU_BLK] = un.blk;
+                mbar_arrive(bar(T_UNIT_FULL + slot));
+                ++k;
+                if (u < 0) break;
+                if (n == 0) continue;
+                // the resident tiles, once the previous unit's last product
+                // that reads them has completed
+                if (rr > 0 && !mbar_wait(bar(T_R_EMPTY), (rr - 1) & 1, wc, TS_R_EMPTY)) break;
                 mbar_arrive_expect_tx(bar(T_R_FULL), 2 * L::kTile);
 #pragma unroll
                 for (int c = 0; c < D / 64; ++c) {
                     if (MODE == DKDV) {
-                        tma_load_4d(sbase + L::kR1 + c * 16384u, &tmK, bar(T_R_FULL), c * 64, blk * kBlock, hk, b);
-                        tma_load_4d(sbase + L::kR2 + c * 16384u, &tmV, bar(T_R_FULL), c * 64, blk * kBlock, hk, b);
+                        tma_load_4d(sbase + L::kR1 + c * 16384u, &tmK, bar(T_R_FULL), c * 64, un.blk * kBlock, un.hk, un.b);
+                        tma_load_4d(sbase + L::kR2 + c * 16384u, &tmV, bar(T_R_FULL), c * 64, un.blk * kBlock, un.hk, un.b);
                     } else {
-                        tma_load_4d(sbase + L::kR1 + c * 16384u, &tmQ, bar(T_R_FULL), c * 64, blk * kBlock, hq0, b);
-                        tma_load_4d(sbase + L::kR2 + c * 16384u, &tmG, bar(T_R_FULL), c * 64, blk * kBlock, hq0, b);
+                        tma_load_4d(sbase + L::kR1 + c * 16384u, &tmQ, bar(T_R_FULL), c * 64, un.blk * kBlock, un.hq0, un.b);
+                        tma_load_4d(sbase + L::kR2 + c * 16384u, &tmG, bar(T_R_FULL), c * 64, un.blk * kBlock, un.hq0, un.b);
                     }
                 }
-                r_loaded = true;
-            }
-            int i = 0;
-            bool ok = true;
-            for (int g = 0; g < heads && ok; ++g) {
-                VisitSeq v;
-                v.row(p, MODE, b, hq0 + g, blk);
-                for (int k = 0; k < v.np + v.nf; ++k, ++i) {
-                    const bool partial = k < v.np;
-                    const int other = __ldg(partial ? v.part + k : v.full + (k - v.np));
-                    const int s = i % ST;
-                    if (i >= ST && !mbar_wait(bar(T_EMPTY + s), (i / ST - 1) & 1, wc, TS_EMPTY)) {
-                        ok = false;
-                        break;
-                    }
-                    info[4 * s + 0] = other;
-                    info[4 * s + 1] = hq0 + g;
-                    info[4 * s + 2] = partial ? 1 : 0;
-                    const uint32_t st1 = sbase + L::kRing + s * 2 * L::kTile, st2 = st1 + L::kTile;
-                    mbar_arrive_expect_tx(bar(T_FULL + s), 2 * L::kTile + (MODE == DKDV ? 1024u : 0u));
-#pragma unroll
-                    for (int c = 0; c < D / 64; ++c) {
-                        if (MODE == DKDV) {
-                            tma_load_4d(st1 + c * 16384u, &tmQ, bar(T_FULL + s), c * 64, other * kBlock, hq0 + g, b);
-                            tma_load_4d(st2 + c * 16384u, &tmG, bar(T_FULL + s), c * 64, other * kBlock, hq0 + g, b);
-                        } else {
-                            tma_load_4d(st1 + c * 16384u, &tmK, bar(T_FULL + s), c * 64, other * kBlock, hk, b);
-                            tma_load_4d(st2 + c * 16384u, &tmV, bar(T_FULL + s), c * 64, other * kBlock, hk, b);
+                ++rr;
+                for (int g = 0; g < un.heads && ok; ++g) {
+                    VisitSeq v;
+                    v.row(p, MODE, un.b, un.hq0 + g, un.blk);
+                    for (int kv = 0; kv < v.np + v.nf; ++kv, ++i) {
+                        const bool partial = kv < v.np;
+                        const int other = __ldg(partial ? v.part + kv : v.full + (kv - v.np));
+                        const int s = i % ST;
+                        if (i >= ST && !mbar_wait(bar(T_EMPTY + s), (i / ST - 1) & 1, wc, TS_EMPTY)) {
+                            ok = false;
+                            break;
                         }
+                        info[4 * s + 0] = other;
+                        info[4 * s + 1] = un.hq0 + g;
+                        info[4 * s + 2] = partial ? 1 : 0;
+                        const uint32_t st1 = sbase + L::kRing + s * 2 * L::kTile, st2 = st1 + L::kTile;
+                        mbar_arrive_expect_tx(bar(T_FULL + s), 2 * L::kTile + (MODE == DKDV ? 1024u : 0u));
+#pragma unroll
+                        for (int c = 0; c < D / 64; ++c) {
+                            if (MODE == DKDV) {
+                                tma_load_4d(st1 + c * 16384u, &tmQ, bar(T_FULL + s), c * 64, other * kBlock, un.hq0 + g, un.b);
+                                tma_load_4d(st2 + c * 16384u, &tmG, bar(T_FULL + s), c * 64, other * kBlock, un.hq0 + g, un.b);
+                            } else {
+                                tma_load_4d(st1 + c * 16384u, &tmK, bar(T_FULL + s), c * 64, other * kBlock, un.hk, un.b);
+                                tma_load_4d(st2 + c * 16384u, &tmV, bar(T_FULL + s), c * 64, other * kBlock, un.hk, un.b);
+                            }
+                        }
+                        if (MODE == DKDV) {
+                            // -lse log2(e) and -Delta of the visit's 128 query rows
+                            const long long r0 =
+                                ((long long)un.b * p.Hq + un.hq0 + g) * p.bm.nq * 128 + (long long)other * 128;
+                            const uint32_t sst = sbase + L::kStats + s * 1024u;
+                            bulk_load(sst, p.rowstats + rows_pad + r0, 512u, bar(T_FULL + s));
+                            bulk_load(sst + 512u, p.rowstats + r0, 512u, bar(T_FULL + s));
+                        }
+                        last = i;
                     }
-                    if (MODE == DKDV) {
-                        // -lse log2(e) and Delta of the visit's 128 query rows
-                        const long long r0 = ((long long)b * p.Hq + hq0 + g) * p.bm.nq * 128 + (long long)other * 128;
-                        const uint32_t sst = sbase + L::kStats + s * 1024u;
-                        bulk_load(sst, p.rowstats + rows_pad + r0, 512u, bar(T_FULL + s));
-                        bulk_load(sst + 512u, p.rowstats + r0, 512u, bar(T_FULL + s));
-                    }
-                    last = i;
                 }
             }
             // every issued copy lands before the CTA may exit
-            if (r_loaded) tc_drain_wait(bar(T_R_FULL), 0, wc, TS_LOAD_DRAIN);
+            if (rr > 0) tc_drain_wait(bar(T_R_FULL), (rr - 1) & 1, wc, TS_LOAD_DRAIN);
             for (int s = 0; s < ST; ++s) {
                 const int ls = last - (((last - s) % ST + ST) % ST);
                 if (last >= 0 && ls >= 0) tc_drain_wait(bar(T_FULL + s), (ls / ST) & 1, wc, TS_LOAD_DRAIN);
@@ -521,20 +578,32 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                                  (!first || kk > 0) ? 1u : 0u);
             }
         };
-        bool ok = n_visits > 0;
-        if (ok && !mbar_wait_warp(bar(T_R_FULL), 0, wc, TS_R)) ok = false;
-        if (ok && !mbar_wait_warp(bar(T_FULL + 0), 0, wc, TS_FULL)) ok = false;
-        if (ok) {
+        uint32_t k = 0;
+        int i = 0, rr = 0;
+        bool ok = true;
+        while (ok) {
+            const uint32_t slot = k & 1;
+            if (!mbar_wait_warp(bar(T_UNIT_FULL + slot), (k >> 1) & 1, wc, TS_UNIT_FULL)) break;
+            const int u = unit_q[TU_WORDS * slot + TU_UNIT], n = unit_q[TU_WORDS * slot + TU_N];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(T_UNIT_EMPTY + slot));
+            ++k;
+            if (u < 0) break;
+            if (n == 0) continue;
+            if (!mbar_wait_warp(bar(T_R_FULL), rr & 1, wc, TS_R)) break;
+            if (!mbar_wait_warp(bar(T_FULL + i % ST), (i / ST) & 1, wc, TS_FULL)) break;
             tc_fence_after();
-            issue_x(0, 0);
-            issue_x(1, 0);
-            for (int i = 0; i < n_visits && ok; ++i) {
-                const bool more = i + 1 < n_visits;
+            issue_x(0, i);
+            issue_x(1, i);
+            for (int v = 0; v < n && ok; ++v, ++i) {
+                const bool more = v + 1 < n;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     if (!mbar_wait_warp(bar(T_PDS + h), i & 1, wc, TS_PDS)) { ok = false; break; }
+                    if (v == 0 && h == 0 && rr > 0 &&
+                        !mbar_wait_warp(bar(T_ACC_FREE), (rr - 1) & 1, wc, TS_ACC_FREE)) { ok = false; break; }
                     tc_fence_after();
-                    issue_acc(h, i, i == 0 && h == 0);
+                    issue_acc(h, i, v == 0 && h == 0);
                     if (h == 1) mma_commit_elect(bar(T_EMPTY + i % ST));
                     if (more) {
                         if (h == 0) {
@@ -543,10 +612,14 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                             tc_fence_after();
                         }
                         issue_x(h, i + 1);
+                    } else if (h == 1) {
+                        mma_commit_elect(bar(T_R_EMPTY));     // every product reading R1, R2 is issued
                     }
                 }
             }
-            if (ok) mma_commit_elect(bar(T_ACC));
+            if (!ok) break;
+            mma_commit_elect(bar(T_ACC));
+            ++rr;
         }
         mma_commit_elect(bar(T_DRAIN));
         tc_drain_wait(bar(T_DRAIN), 0, wc, TS_DRAIN);
@@ -556,14 +629,6 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         const int h = warp >> 2, wq = warp & 3;
         const int r = wq * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-        const int row = blk * kBlock + r;            // key (dK/dV) or query (dQ) of this thread
-        // dQ: the row's statistics, resident for every visit
-        float nl_row = 0.f, nd_row = 0.f;
-        if (MODE == DQ) {
-            const long long pr = ((long long)b * p.Hq + hq0) * p.bm.nq * 128 + row;
-            nl_row = p.rowstats[rows_pad + pr];
-            nd_row = p.rowstats[pr];
-        }
         ElemConst kc{};
         kc.sl2 = p.scale * kLog2eT;
         if (SCORE == FA_SCORE_SOFTCAP || SCORE == FA_SCORE_ALIBI_SOFTCAP) {
@@ -581,150 +646,164 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             kc.xlim4 = kTanhRange / ci;
             kc.xlim2 = kTanh2Range / ci;
         }
+        uint32_t k = 0;
+        int i = 0, rr = 0, cur_hq = -1;
         bool ok = true;
-        int cur_hq = -1;
-        for (int i = 0; i < n_visits && ok; ++i) {
-            const int s = i % ST;
-            // Both warpgroups work on the same half, warpgroup g on its chunk
-            // g (32 columns); while they turn to the other half, the tensor
-            // pipe runs this half's products and the next visit's S, dP.
+        uint8_t* stage = smem + L::kStage + warp * 32 * L::kStageRow;
+        while (ok) {
+            const uint32_t slot = k & 1;
+            if (!mbar_wait_warp(bar(T_UNIT_FULL + slot), (k >> 1) & 1, wc, TS_UNIT_FULL)) break;
+            const volatile int* qs = unit_q + TU_WORDS * slot;
+            const int u = qs[TU_UNIT], n = qs[TU_N], b = qs[TU_B], hq0 = qs[TU_HQ0], hk = qs[TU_HK], blk = qs[TU_BLK];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(T_UNIT_EMPTY + slot));
+            ++k;
+            if (u < 0) break;
+            const int row = blk * kBlock + r;            // key (dK/dV) or query (dQ) of this thread
+            // dQ: the row's statistics, resident for every visit of the unit
+            float nl_row = 0.f, nd_row = 0.f;
+            if (MODE == DQ) {
+                const long long pr = ((long long)b * p.Hq + hq0) * p.bm.nq * 128 + row;
+                nl_row = p.rowstats[rows_pad + pr];
+                nd_row = p.rowstats[pr];
+            }
+            for (int v = 0; v < n && ok; ++v, ++i) {
+                const int s = i % ST;
+                // Both warpgroups work on the same half, warpgroup g on its
+                // chunk g (32 columns); while they turn to the other half, the
+                // tensor pipe runs this half's products and the next visit's
+                // S, dP.
 #pragma unroll 1
-            for (int hh = 0; hh < 2; ++hh) {
-                if (!mbar_wait_warp(bar(T_SD + hh), i & 1, wc, TS_SD)) { ok = false; break; }
-                if (hh == 0 && !mbar_wait_warp(bar(T_FULL + s), (i / ST) & 1, wc, TS_FULL_E)) { ok = false; break; }
-                tc_fence_after();
-                const int other = info[4 * s + 0], hq = info[4 * s + 1];
-                const bool partial = info[4 * s + 2] != 0;
-                if ((SCORE == FA_SCORE_ALIBI || SCORE == FA_SCORE_ALIBI_SOFTCAP) && hq != cur_hq) {
-                    kc.slope = __ldg(p.score.slopes + hq) * (SCORE == FA_SCORE_ALIBI ? kLog2eT : 1.f);
-                    cur_hq = hq;
-                }
-                const float* sst = reinterpret_cast<const float*>(smem + L::kStats + s * 1024u);
-                const int cb = 64 * hh + 32 * h;              // column of the chunk within the tile
-                const int col0 = other * kBlock + cb;         // query (dK/dV) or key (dQ) index of column 0
-                float x[32], y[32], nl[32], nd[32];
-                {
-                    uint32_t rx[32], ry[32];
-                    tmem_ld32_async(tX1 + lane_off + cb, rx);
-                    tmem_ld32_async(tX2 + lane_off + cb, ry);
-                    // the columns' statistics while the loads are in flight
-                    if (MODE == DKDV) {
-                        const float4* n4 = reinterpret_cast<const float4*>(sst + cb);
-                        const float4* d4 = reinterpret_cast<const float4*>(sst + 128 + cb);
+                for (int hh = 0; hh < 2; ++hh) {
+                    if (!mbar_wait_warp(bar(T_SD + hh), i & 1, wc, TS_SD)) { ok = false; break; }
+                    if (hh == 0 && !mbar_wait_warp(bar(T_FULL + s), (i / ST) & 1, wc, TS_FULL_E)) { ok = false; break; }
+                    tc_fence_after();
+                    const int other = info[4 * s + 0], hq = info[4 * s + 1];
+                    const bool partial = info[4 * s + 2] != 0;
+                    if ((SCORE == FA_SCORE_ALIBI || SCORE == FA_SCORE_ALIBI_SOFTCAP) && hq != cur_hq) {
+                        kc.slope = __ldg(p.score.slopes + hq) * (SCORE == FA_SCORE_ALIBI ? kLog2eT : 1.f);
+                        cur_hq = hq;
+                    }
+                    const float* sst = reinterpret_cast<const float*>(smem + L::kStats + s * 1024u);
+                    const int cb = 64 * hh + 32 * h;              // column of the chunk within the tile
+                    const int col0 = other * kBlock + cb;         // query (dK/dV) or key (dQ) index of column 0
+                    float x[32], y[32], nl[32], nd[32];
+                    {
+                        uint32_t rx[32], ry[32];
+                        tmem_ld32_async(tX1 + lane_off + cb, rx);
+                        tmem_ld32_async(tX2 + lane_off + cb, ry);
+                        // the columns' statistics while the loads are in flight
+                        if (MODE == DKDV) {
+                            const float4* n4 = reinterpret_cast<const float4*>(sst + cb);
+                            const float4* d4 = reinterpret_cast<const float4*>(sst + 128 + cb);
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            const float4 a = n4[q], bb = d4[q];
-                            nl[4 * q] = a.x; nl[4 * q + 1] = a.y; nl[4 * q + 2] = a.z; nl[4 * q + 3] = a.w;
-                            nd[4 * q] = bb.x; nd[4 * q + 1] = bb.y; nd[4 * q + 2] = bb.z; nd[4 * q + 3] = bb.w;
+                            for (int q = 0; q < 8; ++q) {
+                                const float4 a = n4[q], bb = d4[q];
+                                nl[4 * q] = a.x; nl[4 * q + 1] = a.y; nl[4 * q + 2] = a.z; nl[4 * q + 3] = a.w;
+                                nd[4 * q] = bb.x; nd[4 * q + 1] = bb.y; nd[4 * q + 2] = bb.z; nd[4 * q + 3] = bb.w;
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) {
+                                nl[e] = nl_row;
+                                nd[e] = nd_row;
+                            }
                         }
-                    } else {
+                        tmem_wait_ld(rx);
+                        tmem_wait_ld(ry);
 #pragma unroll
                         for (int e = 0; e < 32; ++e) {
-                            nl[e] = nl_row;
-                            nd[e] = nd_row;
+                            x[e] = __uint_as_float(rx[e]);
+                            y[e] = __uint_as_float(ry[e]);
                         }
                     }
-                    tmem_wait_ld(rx);
-                    tmem_wait_ld(ry);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        x[e] = __uint_as_float(rx[e]);
-                        y[e] = __uint_as_float(ry[e]);
+                    // i - j of column e is sgn (d0 + e)
+                    const int d0 = col0 - row, sgn = MODE == DKDV ? 1 : -1;
+                    if (partial) {
+                        const uint32_t vmask = chunk_mask<MODE>(p, b, row, col0);
+                        elem_chunk<SCORE, true>(p, hq, kc, x, y, nl, nd, vmask, d0, sgn);
+                    } else {
+                        elem_chunk<SCORE, false>(p, hq, kc, x, y, nl, nd, 0xffffffffu, d0, sgn);
                     }
-                }
-                // i - j of column e is sgn (d0 + e)
-                const int d0 = col0 - row, sgn = MODE == DKDV ? 1 : -1;
-                if (partial) {
-                    const uint32_t vmask = chunk_mask<MODE>(p, b, row, col0);
-                    elem_chunk<SCORE, true>(p, hq, kc, x, y, nl, nd, vmask, d0, sgn);
-                } else {
-                    elem_chunk<SCORE, false>(p, hq, kc, x, y, nl, nd, 0xffffffffu, d0, sgn);
-                }
-                uint32_t pk[16], dk[16];
+                    uint32_t pk[16], dk[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    pk[e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
-                    dk[e] = pack_bf16x2(y[2 * e], y[2 * e + 1]);
+                    for (int e = 0; e < 16; ++e) {
+                        pk[e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
+                        dk[e] = pack_bf16x2(y[2 * e], y[2 * e + 1]);
+                    }
+                    // P (dK/dV only) and dS into the first 16 columns of the
+                    // chunk's own 32 (read above by this warp only)
+                    if (MODE == DKDV) tmem_st16_nowait(tX1 + lane_off + cb, pk);
+                    tmem_st16_nowait(tX2 + lane_off + cb, dk);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(T_PDS + hh));
                 }
-                // P (dK/dV only) and dS into the first 16 columns of the
-                // chunk's own 32 (read above by this warp only)
-                if (MODE == DKDV) tmem_st16_nowait(tX1 + lane_off + cb, pk);
-                tmem_st16_nowait(tX2 + lane_off + cb, dk);
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(T_PDS + hh));
             }
-        }
-        // ---------------------------------------------------------- epilogue
-        // dK/dV: warpgroup 0 writes dV (A1), warpgroup 1 dK (A2, times scale);
-        // dQ: warpgroup h writes columns [h D/2, (h + 1) D/2) of dQ (A1, times
-        // scale).  Rows past the sequence are not written; a block no visit
-        // reached gets zeros.
-        if (ok && n_visits > 0) {
-            if (!mbar_wait_warp(bar(T_ACC), 0, wc, TS_ACC)) ok = false;
-            tc_fence_after();
-        }
-        if (ok) {
+            if (!ok) break;
+            // ------------------------------------------------------ epilogue
+            // dK/dV: warpgroup 0 writes dV (A1), warpgroup 1 dK (A2, times
+            // scale); dQ: warpgroup h writes columns [h D/2, (h + 1) D/2) of
+            // dQ (A1, times scale).  The accumulators are read in one batch,
+            // then released to the next unit (ACC_FREE) before the stores.
+            // Rows past the sequence are not written; a block no visit
+            // reached gets zeros.
             float* out;
             uint32_t tacc;
-            int ncol, col_base, nrows;
+            int col_base, nrows;
             float mul;
             if (MODE == DKDV) {
-                out = h == 0 ? p.dv : p.dk;
+                out = (h == 0 ? p.dv : p.dk) + (((size_t)b * p.Hkv + hk) * p.kv_len) * D;
                 tacc = h == 0 ? tA1 : tA2;
-                ncol = D;
                 col_base = 0;
                 mul = h == 0 ? 1.f : DsSign<SCORE>::kValue * p.scale;   // the elementwise step keeps +-dS
-                out += (((size_t)b * p.Hkv + hk) * p.kv_len) * D;
                 nrows = p.kv_len;
             } else {
                 out = p.dq + (((size_t)b * p.Hq + hq0) * p.q_len) * D;
                 tacc = tA1;
-                ncol = D / 2;
                 col_base = h * (D / 2);
-                mul = DsSign<SCORE>::kValue * p.scale;                  // the elementwise step keeps +-dS
+                mul = DsSign<SCORE>::kValue * p.scale;
                 nrows = p.q_len;
             }
-            // staging rows of this warp (the ring is idle: every product has
-            // completed and every copy has landed)
-            uint8_t* stage = smem + L::kRing + warp * 32 * L::kStageRow;
-            const int rows_left = nrows - (blk * kBlock + wq * 32);
-            // the row's accumulator columns in one batch of loads and one wait
-            constexpr int kMaxChunks = D / 32;
-            uint32_t acc[kMaxChunks][32];
-            const int nch = ncol / 32;
-            if (n_visits > 0) {
+            constexpr int kCh = MODE == DKDV ? D / 32 : D / 64;     // 32-column chunks of this warp
+            uint32_t acc[kCh][32];
+            if (n > 0) {
+                if (!mbar_wait_warp(bar(T_ACC), rr & 1, wc, TS_ACC)) { ok = false; break; }
+                tc_fence_after();
 #pragma unroll
-                for (int c = 0; c < kMaxChunks; ++c)
-                    if (c < nch) tmem_ld32_async(tacc + lane_off + col_base + 32u * c, acc[c]);
+                for (int c = 0; c < kCh; ++c) tmem_ld32_async(tacc + lane_off + col_base + 32u * c, acc[c]);
 #pragma unroll
-                for (int c = 0; c < kMaxChunks; ++c)
-                    if (c < nch) tmem_wait_ld(acc[c]);
+                for (int c = 0; c < kCh; ++c) tmem_wait_ld(acc[c]);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(T_ACC_FREE));
+                ++rr;
             } else {
 #pragma unroll
-                for (int c = 0; c < kMaxChunks; ++c)
+                for (int c = 0; c < kCh; ++c)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) acc[c][e] = 0u;
             }
+            const int rows_left = nrows - (blk * kBlock + wq * 32);
 #pragma unroll
-            for (int c = 0; c < kMaxChunks; ++c) {
-                if (c >= nch) break;
-                const uint32_t (&v)[32] = acc[c];
+            for (int c = 0; c < 2 * kCh; ++c) {            // 16-column pieces through the staging rows
                 __syncwarp();
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t* src = &acc[c >> 1][16 * (c & 1) + 4 * q];
                     *reinterpret_cast<float4*>(stage + lane * L::kStageRow + 16 * q) =
-                        make_float4(__uint_as_float(v[4 * q]) * mul, __uint_as_float(v[4 * q + 1]) * mul,
-                                    __uint_as_float(v[4 * q + 2]) * mul, __uint_as_float(v[4 * q + 3]) * mul);
+                        make_float4(__uint_as_float(src[0]) * mul, __uint_as_float(src[1]) * mul,
+                                    __uint_as_float(src[2]) * mul, __uint_as_float(src[3]) * mul);
+                }
                 __syncwarp();
 #pragma unroll
-                for (int it = 0; it < 8; ++it) {
-                    const int rr = it * 4 + (lane >> 3), piece = lane & 7;
-                    if (rr < rows_left) {
-                        const float4 val = *reinterpret_cast<const float4*>(stage + rr * L::kStageRow + 16 * piece);
-                        const size_t grow = (size_t)(blk * kBlock + wq * 32 + rr);
-                        *reinterpret_cast<float4*>(out + grow * D + col_base + 32 * c + 4 * piece) = val;
+                for (int it = 0; it < 4; ++it) {
+                    const int rr2 = it * 8 + (lane >> 2), piece = lane & 3;
+                    if (rr2 < rows_left) {
+                        const float4 val = *reinterpret_cast<const float4*>(stage + rr2 * L::kStageRow + 16 * piece);
+                        const size_t grow = (size_t)(blk * kBlock + wq * 32 + rr2);
+                        *reinterpret_cast<float4*>(out + grow * D + col_base + 16 * c + 4 * piece) = val;
                     }
                 }
             }
@@ -735,6 +814,16 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, kTcTmemCols);
+    }
+    if (threadIdx.x == 256 + 32 && p.ws) {
+        // The last CTA out resets the unit counter for the next launch on
+        // the same workspace (the dQ kernel, or the next backward).
+        __threadfence();
+        if (atomicAdd(p.ws + WS_SCHED_DONE, 1u) == gridDim.x - 1) {
+            atomicExch(p.ws + WS_SCHED_NEXT, 0u);
+            atomicExch(p.ws + WS_SCHED_DONE, 0u);
+            __threadfence();
+        }
     }
 }
 
@@ -754,15 +843,21 @@ cudaError_t launch_tc_score(const BwdParams& p, const CUtensorMap& tq, const CUt
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
-    // kv blocks (dK/dV) and q-blocks (dQ) in the slow grid dimension, lowest
-    // first: under causal masks those have the most visits, so the longest
-    // CTAs start first
-    bwd_tc_kernel<D, SCORE, DKDV><<<dim3((unsigned)(p.B * p.Hkv), (unsigned)p.bm.nkv), kTcThreads, smem, s>>>(
-        tq, tk, tv, tg, p);
+    // persistent: one CTA per SM (or fewer if there are fewer units)
+    static int sm_count[64] = {};
+    int sms = 148;
+    if (dev >= 0 && dev < 64) {
+        if (sm_count[dev] == 0) {
+            e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+            if (e != cudaSuccess) return e;
+        }
+        sms = sm_count[dev];
+    }
+    const int units_kv = p.B * p.Hkv * p.bm.nkv, units_q = p.B * p.Hq * p.bm.nq;
+    bwd_tc_kernel<D, SCORE, DKDV><<<(unsigned)std::min(units_kv, sms), kTcThreads, smem, s>>>(tq, tk, tv, tg, p, units_kv);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    bwd_tc_kernel<D, SCORE, DQ><<<dim3((unsigned)(p.B * p.Hq), (unsigned)p.bm.nq), kTcThreads, smem, s>>>(
-        tq, tk, tv, tg, p);
+    bwd_tc_kernel<D, SCORE, DQ><<<(unsigned)std::min(units_q, sms), kTcThreads, smem, s>>>(tq, tk, tv, tg, p, units_q);
     return cudaGetLastError();
 }
 
