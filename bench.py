@@ -267,43 +267,76 @@ class Runner:
         return self.time_graph(step_g, steps, warmup, flush), self.time_graph(fwd_g, steps, warmup, flush)
 
     def e2e(self, steps, warmup):
-        """Metric through the public API with pinned host buffers: H2D of the
-        step's inputs, build + forward, D2H of O and lse, every step."""
+        """Metric through the public API with pinned host buffers: every step
+        copies its inputs host -> device, builds the BlockMask, runs the
+        forward and copies O and lse device -> host.  Steps are pipelined over
+        three streams with two buffer sets: step i+1's inputs go up while step
+        i computes and step i-1's result comes down (the two copy directions
+        of the host link run at once)."""
         torch, w = self.torch, self.w
         hq, hk, hv = (torch.from_numpy(x).to(self.dt).pin_memory() for x in self.host)
         hseg = torch.from_numpy(self.seg).pin_memory() if self.seg is not None else None
-        ho = torch.empty(self.q.shape, dtype=self.dt).pin_memory()
-        hl = torch.empty(self.lse.shape, dtype=torch.float32).pin_memory()
+        ho = [torch.empty(self.q.shape, dtype=self.dt).pin_memory() for _ in range(2)]
+        hl = [torch.empty(self.lse.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
         slopes = self.score_kw.get("alibi_slopes")
         hsl = slopes.cpu().pin_memory() if slopes is not None else None
         h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv) + ((hseg,) if hseg is not None else ())
                   + ((hsl,) if hsl is not None else ()))
-        d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+        d2h = ho[0].numel() * ho[0].element_size() + hl[0].numel() * hl[0].element_size()
+        dev = self.device
+        up, comp, down = (torch.cuda.Stream(device=dev) for _ in range(3))
+        bufs = []
+        for _ in range(2):
+            d = {"q": torch.empty_like(self.q), "k": torch.empty_like(self.k), "v": torch.empty_like(self.v),
+                 "o": torch.empty_like(self.q), "lse": torch.empty_like(self.lse),
+                 "seg": torch.empty_like(self.seg_d) if self.seg_d is not None else None,
+                 "slopes": torch.empty_like(slopes) if slopes is not None else None,
+                 "ws": self.fa.Workspace(dev)}
+            bufs.append(d)
+        ev_up = [torch.cuda.Event() for _ in range(2)]
+        ev_comp = [torch.cuda.Event() for _ in range(2)]
+        ev_down = [torch.cuda.Event() for _ in range(2)]
+        Bm = self.seg.shape[0] if self.seg is not None else 1
 
-        def one():
-            q = hq.to(self.device, non_blocking=True)
-            k = hk.to(self.device, non_blocking=True)
-            v = hv.to(self.device, non_blocking=True)
-            seg = hseg.to(self.device, non_blocking=True) if hseg is not None else None
-            kw = dict(self.score_kw)
-            if hsl is not None:
-                kw["alibi_slopes"] = hsl.to(self.device, non_blocking=True)
-            Bm = seg.shape[0] if seg is not None else 1
-            bm = self.fa.block_mask(w.mask, Bm, 1, w.T, w.T, window=w.window, prefix_len=w.prefix_len,
-                                    seg_ids=seg, workspace=self.ws)
-            o, lse = self.fa.fwd(q, k, v, bm, workspace=self.ws, **kw)
-            ho.copy_(o, non_blocking=True)
-            hl.copy_(lse, non_blocking=True)
+        def step(i):
+            d, j = bufs[i % 2], i % 2
+            with torch.cuda.stream(up):
+                up.wait_event(ev_comp[j])          # the compute of step i-2 is done with these inputs
+                d["q"].copy_(hq, non_blocking=True)
+                d["k"].copy_(hk, non_blocking=True)
+                d["v"].copy_(hv, non_blocking=True)
+                if hseg is not None:
+                    d["seg"].copy_(hseg, non_blocking=True)
+                if hsl is not None:
+                    d["slopes"].copy_(hsl, non_blocking=True)
+                ev_up[j].record(up)
+            with torch.cuda.stream(comp):
+                comp.wait_event(ev_up[j])
+                comp.wait_event(ev_down[j])        # step i-2's output has left this buffer
+                kw = dict(self.score_kw)
+                if hsl is not None:
+                    kw["alibi_slopes"] = d["slopes"]
+                bm = self.fa.block_mask(w.mask, Bm, 1, w.T, w.T, window=w.window, prefix_len=w.prefix_len,
+                                        seg_ids=d["seg"], workspace=d["ws"], stream=comp)
+                self.fa.fwd(d["q"], d["k"], d["v"], bm, out=d["o"], lse=d["lse"], workspace=d["ws"],
+                            stream=comp, **kw)
+                ev_comp[j].record(comp)
+            with torch.cuda.stream(down):
+                down.wait_event(ev_comp[j])
+                ho[j].copy_(d["o"], non_blocking=True)
+                hl[j].copy_(d["lse"], non_blocking=True)
+                ev_down[j].record(down)
 
-        for _ in range(warmup):
-            one()
+        for i in range(warmup):
+            step(i)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        for _ in range(steps):
-            one()
+        for i in range(steps):
+            step(warmup + i)
         torch.cuda.synchronize()
         sec = (time.perf_counter() - t0) / steps
-        self.ws.check()
+        for d in bufs:
+            d["ws"].check()
         return sec, h2d, d2h
 
 
