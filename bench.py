@@ -422,14 +422,18 @@ def summarize(w, r, step_ms, fwd_ms, peaks, peak_src, build_ms=None, floor_ms=No
 
 
 def compact(entry, tc_peak):
-    """The few numbers of a workload the last lines of the output keep."""
+    """The few numbers of a workload the last lines of the output keep:
+    kernel ms, the roofline fraction keyed by its bound ("tensor" of the
+    cuBLAS peak, "tc05" of the tcgen05 issue rate, "hbm" of the copy
+    bandwidth, "floor" the launch floor over the time), and the builder's
+    HBM fraction ("build")."""
     roof = entry["roofline"]
-    c = {"fwd_ms": entry["fwd_ms"], "bound": roof["bound"], "frac": roof["frac"]}
+    key = {"tensor": "tensor", "hbm": "hbm", "latency": "floor"}.get(roof["bound"], roof["bound"])
+    c = {"ms": entry["fwd_ms"], key: roof["frac"] if roof["frac"] is None else round(roof["frac"], 3)}
     if roof["bound"] == "tensor" and tc_peak:
-        c["frac_tcgen05"] = round(roof["achieved"] / tc_peak, 4)
+        c["tc05"] = round(roof["achieved"] / tc_peak, 3)
     if "build" in entry:
-        c["build_ms"] = entry["build"]["build_ms"]
-        c["build_frac"] = entry["build"]["frac"]
+        c["build"] = round(entry["build"]["frac"], 3)
     return c
 
 
@@ -859,12 +863,11 @@ def main():
         for name, entry in secondary.items():
             summary[name] = compact(entry, tc_peak)
         if build_scale:
-            summary["block_mask_build_16x131072"] = {"build_ms": build_scale["build_ms"],
-                                                      "bound": "hbm", "frac": build_scale["frac"]}
+            summary["build_16x131072"] = {"ms": build_scale["build_ms"], "hbm": round(build_scale["frac"], 3)}
         for name, entry in (backward or {}).items():
-            summary["bwd_" + name] = {"ms": entry["ms"], "bound": "tensor", "frac": entry["roofline"]["frac"]}
+            summary["bwd_" + name] = {"ms": entry["ms"], "tensor": round(entry["roofline"]["frac"], 3)}
         for name, entry in (decode or {}).items():
-            summary[name] = {"ms": entry["ms"], "bound": "hbm", "frac": entry["roofline"]["frac"]}
+            summary[name] = {"ms": entry["ms"], "hbm": round(entry["roofline"]["frac"], 3)}
         line = {
             "metric": METRIC,
             "value": round(head["tflops"] * n, 3),
