@@ -96,11 +96,12 @@ enum Site : uint32_t { S_Q = 1, S_Q_EMPTY, S_K_FULL, S_K_EMPTY, S_V_FULL, S_V_EM
                        S_O_UPD };
 constexpr uint32_t kUnitConsumers = 10;   // one lane of each MMA warp and of each softmax warp
 // A unit-queue slot: the unit (-1 = none left), whether its pair visits any
-// kv tile, and for each query tile its BlockMask row's list lengths and first
-// entries (read by the loader, so that no other role waits for them).
-constexpr int kUnitWords = 14;
+// kv tile, the unit's batch, query head and pair index, and for each query
+// tile its BlockMask row's list lengths and first entries (read and decoded
+// by the loader, so that no other role waits for them or divides).
+constexpr int kUnitWords = 17;
 // UW_ROW + 6 t + {n_part, n_full, part[n_part - 1], part[n_part - 2], full[n_full - 1], full[n_full - 2]}
-enum UnitWord { UW_UNIT = 0, UW_HAS_STEPS = 1, UW_ROW = 2 };
+enum UnitWord { UW_UNIT = 0, UW_HAS_STEPS = 1, UW_B = 2, UW_HQ = 3, UW_PR = 4, UW_ROW = 5 };
 
 // d = a * b on two lanes at once.
 __device__ __forceinline__ void fmul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
@@ -165,7 +166,8 @@ __device__ __forceinline__ void exp_pair(float& p0, float& p1, float x0, float x
 // argument, x Q(x^2) + nm (TIER 2 or 4: the folded polynomial of that degree,
 // coefficients k0..k4; TIER 0: the exact form), P packed to bf16 into TMEM
 // (its first 32 columns) and the row sums into rs.  PARTIAL: elements with
-// x = -inf give exactly 0.
+// x = -inf are forced to 0 (the exact form needs it; the polynomials give 0
+// for them by themselves).
 template <int TIER, bool PARTIAL>
 __device__ __forceinline__ void softcap_exp_half(const float (&x)[64], float nm, float k0, float k1, float k2,
                                                  float k3, float k4, float cap_in, float cap_out, uint32_t tP,
@@ -447,6 +449,9 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 qs[UW_UNIT] = u;
                 qs[UW_HAS_STEPS] = u >= 0 && !seq.empty();
                 if (u >= 0) {
+                    qs[UW_B] = pu.b;
+                    qs[UW_HQ] = pu.hq;
+                    qs[UW_PR] = pu.pr;
 #pragma unroll
                     for (int t = 0; t < 2; ++t) {
                         qs[UW_ROW + 6 * t + 0] = seq.row[t].n_part();
@@ -571,6 +576,11 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             // S_t,h = Q_t K(step gg, rows 64 h .. 64 h + 63)^T: N = 64, K = D in
             // steps of 16 (32 bytes inside the 128-byte swizzled row; the next
             // 64-column block 16 KB on).
+            // The halves below are rolled loops: the MMA warps share their SM
+            // sub-partitions' instruction caches with the softmax warps, so
+            // their code is kept small (a copy of the 12 MMAs of a half per
+            // call site cost 11 % on the causal soft-cap workload).  The K
+            // steps stay unrolled: a rolled issue loop delays S.
             auto issue_qk = [&](int h, uint32_t gg) {
                 const uint64_t kd = k_desc0 + (((gg % ST) * L::kTile + 8192u * h) >> 4);
 #pragma unroll
@@ -625,8 +635,8 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 if (f & in_t) {
                     if (!need_q()) break;
                     tc_fence_after();
-                    issue_qk(0, g);
-                    issue_qk(1, g);
+#pragma unroll 1
+                    for (int h = 0; h < 2; ++h) issue_qk(h, g);
                     if (f & last_t) mma_commit_elect(bar(B_Q_EMPTY + t));
                 }
                 mma_commit_elect(bar(B_K_EMPTY + g % ST));
@@ -651,7 +661,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     // arrive on the stage's next phase.
                     if (!mbar_wait_warp(bar(B_V_FULL + g % ST), (g / ST) & 1, wc, S_V_FULL)) { ok = false; break; }
                     if (f & in_t) {
-#pragma unroll
+#pragma unroll 1
                         for (int h = 0; h < 2; ++h) {
                             if (!mbar_wait_warp(bar(B_P_FULL + 2 * t + h), np & 1, wc, S_P_FULL)) { ok = false; break; }
                             tc_fence_after();
@@ -672,8 +682,8 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         if (fn & in_t) {
                             if (!need_q()) { ok = false; break; }
                             tc_fence_after();
-                            issue_qk(0, g1);
-                            issue_qk(1, g1);
+#pragma unroll 1
+                            for (int h = 0; h < 2; ++h) issue_qk(h, g1);
                         }
                     }
                     if (more && (fn & last_t)) mma_commit_elect(bar(B_Q_EMPTY + t));
@@ -763,7 +773,9 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             c.u = qs[UW_UNIT];
             c.qb = 0;
             if (c.u >= 0) {
-                c.pu = decode_pair(p, c.u);
+                c.pu.b = qs[UW_B];
+                c.pu.hq = qs[UW_HQ];
+                c.pu.pr = qs[UW_PR];
                 c.qb = 2 * c.pu.pr + t;
                 c.rs.init_from(p, c.pu.b, c.pu.hq, c.qb, qs + UW_ROW + 6 * t);
             }
@@ -1020,12 +1032,13 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         // P = 2^(cap(x) - m): the capped score formed in the
                         // exponent's argument; masked elements (x = -inf) give 0
                         const uint32_t tPh = tSh + lane_off;
+                        // The polynomials need no mask test: their leading
+                        // coefficients are positive (scale and C are), so a
+                        // masked x = -inf gives Q = +inf, x Q = -inf and P = 0.
                         if (tier == 2) {
-                            if (partial) softcap_exp_half<2, true>(x, nm, tr0, tr1, tr2, 0.f, 0.f, cap_in, cap_out, tPh, rs);
-                            else softcap_exp_half<2, false>(x, nm, tr0, tr1, tr2, 0.f, 0.f, cap_in, cap_out, tPh, rs);
+                            softcap_exp_half<2, false>(x, nm, tr0, tr1, tr2, 0.f, 0.f, cap_in, cap_out, tPh, rs);
                         } else if (tier == 4) {
-                            if (partial) softcap_exp_half<4, true>(x, nm, tq0, tq1, tq2, tq3, tq4, cap_in, cap_out, tPh, rs);
-                            else softcap_exp_half<4, false>(x, nm, tq0, tq1, tq2, tq3, tq4, cap_in, cap_out, tPh, rs);
+                            softcap_exp_half<4, false>(x, nm, tq0, tq1, tq2, tq3, tq4, cap_in, cap_out, tPh, rs);
                         } else {
                             softcap_exp_half<0, true>(x, nm, 0.f, 0.f, 0.f, 0.f, 0.f, cap_in, cap_out, tPh, rs);
                         }
@@ -1105,32 +1118,35 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             uint8_t* stage = smem + L::kOStage + warp * 32 * L::kOStageRow;
             const size_t head_row0 = ((size_t)pu.b * p.Hq + pu.hq) * p.q_len;
             const int rows_left = p.q_len - (qb * kBlock + wq * 32);   // rows of this warp that exist
-            // The whole row of O comes out of TMEM in one batch of loads and
-            // one wait (a load per chunk with its own wait cost about 1000
-            // cycles each while the tensor pipe runs the other tile's work).
-            uint32_t o[D / 32][32];
-            if (active) {
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) tmem_ld32_async(tO + lane_off + 32u * c, o[c]);
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) tmem_wait_ld(o[c]);
-            } else {
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c)
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) o[c][e] = 0u;
-            }
+            // One 64-byte chunk at a time, each loaded from TMEM when it is
+            // needed: the epilogue runs once per unit, so its code is cold in
+            // the instruction cache, and a rolled loop keeps it to a few lines.
             const int nchunk = out32 ? D / 16 : D / 32;
-#pragma unroll
+#pragma unroll 1
             for (int c = 0; c < nchunk; ++c) {
                 uint32_t w[16];
                 if (out32) {
+                    uint32_t o[16];
+                    if (active) {
+                        tmem_ld16(tO + lane_off + 16u * c, o);
+                    } else {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(__uint_as_float(o[c >> 1][16 * (c & 1) + e]) * inv);
+                        for (int e = 0; e < 16; ++e) o[e] = 0u;
+                    }
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(__uint_as_float(o[e]) * inv);
                 } else {
+                    uint32_t o[32];
+                    if (active) {
+                        tmem_ld32_async(tO + lane_off + 32u * c, o);
+                        tmem_wait_ld(o);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = 0u;
+                    }
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
-                        w[e] = pack_bf16x2(__uint_as_float(o[c][2 * e]) * inv, __uint_as_float(o[c][2 * e + 1]) * inv);
+                        w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
                 }
                 __syncwarp();    // the previous chunk's reads of the staging rows are done
 #pragma unroll
