@@ -627,71 +627,61 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     q_ready = true;
                     return true;
                 };
-                // the first step's products, both halves; each step's flags
-                // come with its K
-                if (!mbar_wait_warp(bar(B_K_FULL + g % ST), (g / ST) & 1, wc, S_K_FULL)) break;
-                uint32_t f = step_flags[g % ST];
-                tc_fence_after();
-                if (f & in_t) {
-                    if (!need_q()) break;
-                    tc_fence_after();
-#pragma unroll 1
-                    for (int h = 0; h < 2; ++h) issue_qk(h, g);
-                    if (f & last_t) mma_commit_elect(bar(B_Q_EMPTY + t));
-                }
-                mma_commit_elect(bar(B_K_EMPTY + g % ST));
-                // Step g: for each half h, O_t += P_t,h V(g) and then, into the
-                // S buffer that product has just released, S_t,h = Q_t K(g + 1)
-                // for the next step.
+                // One pass per step g of the unit, plus one after the last:
+                // for each half h, O_t += P_t,h V(g - 1) (if tile t visits
+                // step g - 1) and then, into the S buffer that product has
+                // just released, S_t,h = Q_t K(g) (if it visits step g).  Each
+                // product has a single call site, which keeps the warp's code
+                // small.  A step's flags come with its K.
+                bool prev = false;          // step g - 1 of this unit exists (flags fp)
+                bool more = true;           // step g exists
+                uint32_t fp = 0;
                 while (true) {
-                    const bool more = !(f & kLastOfUnit);
-                    const uint32_t g1 = g + 1;
                     uint32_t fn = 0;
                     bool k_ready = !more;
                     auto need_k = [&]() -> bool {
                         if (k_ready) return true;
-                        if (!mbar_wait_warp(bar(B_K_FULL + g1 % ST), (g1 / ST) & 1, wc, S_K_FULL)) return false;
-                        fn = step_flags[g1 % ST];
+                        if (!mbar_wait_warp(bar(B_K_FULL + g % ST), (g / ST) & 1, wc, S_K_FULL)) return false;
+                        fn = step_flags[g % ST];
                         k_ready = true;
                         return true;
                     };
-                    // Both warps wait for V(g) (and for K of every step), even
+                    const uint32_t gp = g - 1;
+                    // Both warps wait for V of every step (and for K), even
                     // where their tile does not visit the step: a stage's
                     // barrier phase then completes before either warp can
                     // arrive on the stage's next phase.
-                    if (!mbar_wait_warp(bar(B_V_FULL + g % ST), (g / ST) & 1, wc, S_V_FULL)) { ok = false; break; }
-                    if (f & in_t) {
+                    if (prev && !mbar_wait_warp(bar(B_V_FULL + gp % ST), (gp / ST) & 1, wc, S_V_FULL)) { ok = false; break; }
+                    const bool pv = prev && (fp & in_t);
 #pragma unroll 1
-                        for (int h = 0; h < 2; ++h) {
+                    for (int h = 0; h < 2; ++h) {
+                        if (pv) {
                             if (!mbar_wait_warp(bar(B_P_FULL + 2 * t + h), np & 1, wc, S_P_FULL)) { ok = false; break; }
                             tc_fence_after();
-                            issue_pv(h, g, started);
+                            issue_pv(h, gp, started);
                             started = true;
-                            if (!need_k()) { ok = false; break; }
-                            if (fn & in_t) {
-                                if (!need_q()) { ok = false; break; }
-                                tc_fence_after();
-                                issue_qk(h, g1);
-                            }
                         }
-                        if (!ok) break;
-                        ++np;
-                        if (f & last_t) mma_commit_elect(bar(B_O_DONE + t));
-                    } else {
+                        // K(g) is waited for after the first P V of the pass
                         if (!need_k()) { ok = false; break; }
                         if (fn & in_t) {
                             if (!need_q()) { ok = false; break; }
                             tc_fence_after();
-#pragma unroll 1
-                            for (int h = 0; h < 2; ++h) issue_qk(h, g1);
+                            issue_qk(h, g);
                         }
                     }
-                    if (more && (fn & last_t)) mma_commit_elect(bar(B_Q_EMPTY + t));
-                    mma_commit_elect(bar(B_V_EMPTY + g % ST));
-                    if (more) mma_commit_elect(bar(B_K_EMPTY + g1 % ST));
-                    g = g1;
+                    if (!ok) break;
+                    if (pv) {
+                        ++np;
+                        if (fp & last_t) mma_commit_elect(bar(B_O_DONE + t));
+                    }
+                    if (fn & last_t) mma_commit_elect(bar(B_Q_EMPTY + t));
+                    if (prev) mma_commit_elect(bar(B_V_EMPTY + gp % ST));
+                    if (more) mma_commit_elect(bar(B_K_EMPTY + g % ST));
                     if (!more) break;
-                    f = fn;
+                    prev = true;
+                    fp = fn;
+                    more = !(fn & kLastOfUnit);
+                    ++g;
                 }
                 if (!ok) break;
                 if (q_ready) ++uq;
