@@ -153,6 +153,15 @@ __device__ __forceinline__ void seg_bounds_warp(const int (&ids)[4], int key, in
     }
 }
 
+// Whether some row of the warp sees a column of a partial half (columns
+// ch .. ch + 63) under a document mask: the row's visible tile columns are
+// [seg_lo, seg_hi], and none past kv_len.
+__device__ __forceinline__ bool doc_half_seen(int kv_len, int ch, int h, int seg_lo, int seg_hi) {
+    const int lo = seg_lo - 64 * h;
+    const int hi = min(min(63, kv_len - 1 - ch), seg_hi - 64 * h);
+    return __any_sync(0xffffffffu, lo <= 63 && hi >= 0 && lo <= hi);
+}
+
 // One pair of probabilities: p = 2^(x * sc - m) on the MUFU ex2 unit.
 __device__ __forceinline__ void exp_pair(float& p0, float& p1, float x0, float x1, float sc, float nm) {
     float a0, a1;
@@ -840,6 +849,25 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         tw0 = __ldg(tab_row + (ch >> 5));
                         if (ch + 32 < p.kv_len) tw1 = __ldg(tab_row + (ch >> 5) + 1);
                     }
+                    // A partial half that no row of the warp sees (most halves
+                    // off the diagonal under group and document masks): P = 0
+                    // without reading S; the running max and sum stay.  Only
+                    // document masks take the test: the causal and window
+                    // kernels ran 1.5 % slower with it.
+                    if (__builtin_expect(doc && partial && !doc_half_seen(p.kv_len, ch, h, seg_lo, seg_hi), 0)) {
+                        if (!mbar_wait_warp(bar(B_S_FULL + 2 * t + h), n & 1, wc, S_S_FULL)) { ok = false; break; }
+                        tc_fence_after();
+                        uint32_t zero[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) zero[e] = 0u;
+                        tmem_st16_nowait(tSh + lane_off, zero);
+                        tmem_st16_nowait(tSh + lane_off + 16u, zero);
+                        tmem_wait_st();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar(B_P_FULL + 2 * t + h));
+                        continue;
+                    }
                     if (!mbar_wait_warp(bar(B_S_FULL + 2 * t + h), n & 1, wc, S_S_FULL)) { ok = false; break; }
                     tc_fence_after();
                     float x[64];
@@ -1004,16 +1032,17 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     const float m_new = fmaxf(m_use, mx);
                     // A lazy max (bf16 output): O and l follow the max only
                     // when it grows by more than kLazyMax (base 2), so P may
-                    // reach 2^kLazyMax; the first half of a unit sets it.
+                    // reach 2^kLazyMax; the first half in which the row sees
+                    // a key sets it (O and l are still 0 then: no rescale).
                     // O = (P V) / l then carries the bf16 rounding of the
                     // largest P, at most 2^-9 max|V|, the size of the bf16
                     // output's own rounding.  With fp32 output the max is
                     // exact (lazy = 0): the largest P is 1 and rounds exactly.
-                    const bool first = j == 0 && h == 0;
-                    const bool need = !first && m_new > m_use + lazy;
+                    const bool unset = m_use == -CUDART_INF_F;
+                    const bool need = !unset && m_new > m_use + lazy;
                     const float alpha = need ? ex2_approx(m_use - m_new) : 1.f;
                     if (need) l *= alpha;
-                    if (first || need) m_use = m_new;
+                    if (unset || need) m_use = m_new;
                     const float nm = m_use == -CUDART_INF_F ? 0.f : -m_use;
 
                     // P = 2^(x sc - m) -> bf16 pairs into TMEM over S_t,h
