@@ -442,14 +442,18 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             uint32_t k = 0, g = 0, uq[2] = {0u, 0u};
             int last_q[2] = {-1, -1}, last_k = -1, last_v = -1;
             bool ok = true;
-            while (ok) {
+            // Claims a unit from the counter and publishes it in the next
+            // queue slot (-1: none left).  The unit after the current one is
+            // published as soon as the current one's loads reach its last
+            // step, so that the other roles find it there when they finish
+            // the current one, instead of waiting for this lane's last ring
+            // waits, the counter and the BlockMask reads.
+            auto publish = [&](int& u, Pair& pu, PairSeq& seq) -> bool {
                 const uint32_t slot = k & 1;
                 if (k >= 2 && !mbar_wait(bar(B_UNIT_EMPTY + slot), ((k >> 1) - 1) & 1, wc, S_UNIT_EMPTY))
-                    break;
-                int u = static_cast<int>(atomicAdd(p.ws + WS_SCHED_NEXT, 1u));
+                    return false;
+                u = static_cast<int>(atomicAdd(p.ws + WS_SCHED_NEXT, 1u));
                 if (u >= p.num_units) u = -1;
-                Pair pu{};
-                PairSeq seq;
                 if (u >= 0) {
                     pu = decode_pair(p, u);
                     seq.init(p, pu);
@@ -473,6 +477,14 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 }
                 mbar_arrive(bar(B_UNIT_FULL + slot));
                 ++k;
+                return true;
+            };
+            int u = -1;
+            Pair pu{};
+            PairSeq seq;
+            bool have = false;      // u was published at the previous unit's last step
+            while (ok) {
+                if (!have && !publish(u, pu, seq)) break;   // the first unit, or after one without steps
                 if (u < 0) break;
                 // This unit's Q tiles and first K / V tiles go to L2 now: the
                 // loads below wait for the previous unit to release the Q
@@ -523,9 +535,17 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     last_v = static_cast<int>(gv);
                     return true;
                 };
+                int un = -1;
+                Pair pn{};
+                PairSeq sn;
+                bool published = false;
                 int kb, kb_pend = -1;
                 uint32_t flags;
                 while (ok && seq.next(kb, flags)) {
+                    if ((flags & kLastOfUnit) && !published) {
+                        if (!publish(un, pn, sn)) { ok = false; break; }
+                        published = true;
+                    }
                     const uint32_t s = g % ST;
                     if (g >= ST && !mbar_wait(bar(B_K_EMPTY + s), (g / ST - 1) & 1, wc, S_K_EMPTY)) {
                         ok = false;
@@ -547,6 +567,10 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     ++g;
                 }
                 if (ok && kb_pend >= 0 && !load_v(g - 1, kb_pend)) ok = false;
+                have = published;
+                u = un;
+                pu = pn;
+                seq = sn;
             }
             // Let every issued copy land before the CTA may exit: the last
             // load into each Q buffer and each stage (last_k skips a K load
