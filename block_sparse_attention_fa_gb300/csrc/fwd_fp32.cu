@@ -68,11 +68,15 @@ __global__ void __launch_bounds__(kThreads32) fwd_fp32_kernel(const FwdParams p)
     const float4* k4 = reinterpret_cast<const float4*>(p.k) + ((size_t)b * p.Hkv + hk) * p.kv_len * NV;
     const float4* v4 = reinterpret_cast<const float4*>(p.v) + ((size_t)b * p.Hkv + hk) * p.kv_len * NV;
 
-    // the CTA's Q rows (zeros past q_len)
-    for (int e = tid; e < kRows * NV; e += kThreads32) {
-        const int rr = e / NV, cc = e % NV;
-        const float4 v = cr0 + rr < p.q_len ? q4[(size_t)(cr0 + rr) * NV + cc] : make_float4(0.f, 0.f, 0.f, 0.f);
-        *reinterpret_cast<float4*>(&qs[rr * KP + 4 * cc]) = v;
+    // the CTA's Q rows (zeros past q_len), read now and stored to shared
+    // memory after the BlockMask reads below, so that the two overlap
+    constexpr int kPerQ = (kRows * NV + kThreads32 - 1) / kThreads32;
+    float4 qv[kPerQ];
+#pragma unroll
+    for (int t = 0; t < kPerQ; ++t) {
+        const int e = tid + t * kThreads32, rr = e / NV, cc = e % NV;
+        qv[t] = (e < kRows * NV && cr0 + rr < p.q_len) ? q4[(size_t)(cr0 + rr) * NV + cc]
+                                                       : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 
     const int mb = p.bm.B == 1 ? 0 : b, mh = p.bm.H == 1 ? 0 : hq;
@@ -139,6 +143,11 @@ __global__ void __launch_bounds__(kThreads32) fwd_fp32_kernel(const FwdParams p)
         pos = 0;
     };
     if (n > 0) load_batch(0);
+#pragma unroll
+    for (int t = 0; t < kPerQ; ++t) {
+        const int e = tid + t * kThreads32, rr = e / NV, cc = e % NV;
+        if (e < kRows * NV) *reinterpret_cast<float4*>(&qs[rr * KP + 4 * cc]) = qv[t];
+    }
     auto next_chunk = [&](int& cs, bool& partial) -> bool {
         for (;;) {
             const int total = nb * kSubs;
