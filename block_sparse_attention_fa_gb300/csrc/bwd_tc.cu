@@ -28,10 +28,10 @@
 // S and dP are computed in both kernels so that no gradient needs atomics and
 // the result does not depend on the order of the visits.
 //
-// Roles (320 threads): warps 0-3 and 4-7 are two elementwise warpgroups
-// (thread r of a warpgroup owns TMEM lane r: a key row in the dK/dV kernel, a
-// query row in the dQ kernel; warpgroup g takes columns 32 g .. 32 g + 31 of
-// each half); warp 8 loads with TMA; warp 9 issues the tcgen05 MMAs (one
+// Roles (576 threads): warps 0-15 are four elementwise warpgroups (thread r
+// of a warpgroup owns TMEM lane r: a key row in the dK/dV kernel, a query row
+// in the dQ kernel; warpgroup g takes columns 16 g .. 16 g + 15 of each
+// half); warp 16 loads with TMA; warp 17 issues the tcgen05 MMAs (one
 // elected lane).  The two halves ping-pong: while the warpgroups turn S_h, dP_h
 // into P_h, dS_h, the tensor pipe runs the other half's products.  TMEM (512 columns): S_h at 64 h, dP_h at 128 + 64 h,
 // accumulators at 256 (dV or dQ) and 256 + D (dK).  Every wait is bounded as in
@@ -51,13 +51,15 @@
 namespace fa {
 namespace {
 
-constexpr int kTcThreads = 320;
+constexpr int kTcThreads = 576;
+constexpr int kTcLoader = 16, kTcMma = 17;   // warp indices
+constexpr int kW = 16;                        // columns of a half per elementwise warpgroup
 constexpr uint32_t kTcTmemCols = 512;
 constexpr float kLog2eT = 1.4426950408889634f;
 enum Mode { DKDV = 0, DQ = 1 };
 
 // Barriers: resident tiles; per ring stage FULL and EMPTY; per half h the
-// S_h / dP_h products (SD) and the elementwise results (PDS, all 8 warps);
+// S_h / dP_h products (SD) and the elementwise results (PDS, all 16 warps);
 // accumulation done; the MMA warp's drain.
 constexpr int kMaxSt = 4;
 enum TcBar {
@@ -74,7 +76,7 @@ enum TcSite : uint32_t { TS_R = 101, TS_FULL, TS_EMPTY, TS_SD, TS_PDS, TS_ACC, T
 // A unit-queue slot: the unit (-1: none left), its visit count, b, first
 // query head, kv head, resident block.
 enum TcUnitWord { TU_UNIT = 0, TU_N, TU_B, TU_HQ0, TU_HK, TU_BLK, TU_WORDS = 8 };
-constexpr uint32_t kTcUnitConsumers = 9;    // the MMA warp and the 8 elementwise warps
+constexpr uint32_t kTcUnitConsumers = 17;   // the MMA warp and the 16 elementwise warps
 
 template <int D>
 struct TcLayout {
@@ -84,11 +86,7 @@ struct TcLayout {
     static constexpr uint32_t kRing = 2 * kTile;                 // per stage: streamed tiles 1 and 2
     static constexpr uint32_t kStats = kRing + kStages * 2 * kTile;   // per stage: -lse log2 e [128], Delta [128]
     static constexpr uint32_t kInfo = kStats + kStages * 1024;        // per stage: block, head, partial
-    // epilogue staging: per warp 32 rows x 16 fp32, rows padded to 80 bytes
-    // (its own space: the ring is already taking the next unit's tiles)
-    static constexpr uint32_t kStageRow = 80;
-    static constexpr uint32_t kStage = kInfo + kStages * 16;
-    static constexpr uint32_t kUnitQ = kStage + 8 * 32 * kStageRow;   // 2 slots x TU_WORDS int32
+    static constexpr uint32_t kUnitQ = kInfo + kStages * 16;   // 2 slots x TU_WORDS int32
     static constexpr uint32_t kBars = kUnitQ + 2 * 4 * TU_WORDS;
     static constexpr uint32_t kTmemSlot = kBars + 8 * T_COUNT;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
@@ -179,7 +177,7 @@ struct ElemConst {
     float q0, q1, q2, q3, q4, r0, r1, r2, xlim4, xlim2;
 };
 
-// The elementwise step of 32 consecutive columns of one row.  In: x = raw
+// The elementwise step of kW consecutive columns of one row.  In: x = raw
 // q.k, y = raw dP (fp32, from TMEM).  Out: x = P (probabilities, 0 where
 // masked), y = dS = P (dP - Delta) d score_mod / d s, or -dS for the
 // soft-cap score_mods (one operation fewer; kDsSign gives the sign, which
@@ -196,14 +194,14 @@ struct DsSign {
 };
 
 template <int SCORE, bool PARTIAL>
-__device__ __forceinline__ void elem_chunk(const BwdParams& p, int hq, const ElemConst& k, float (&x)[32],
-                                           float (&y)[32], const float (&nl)[32], const float (&nd)[32],
+__device__ __forceinline__ void elem_chunk(const BwdParams& p, int hq, const ElemConst& k, float (&x)[kW],
+                                           float (&y)[kW], const float (&nl)[kW], const float (&nd)[kW],
                                            uint32_t vmask, int d0, int sgn) {
     if (SCORE == FA_SCORE_SOFTCAP || SCORE == FA_SCORE_ALIBI_SOFTCAP) {
         if (SCORE == FA_SCORE_ALIBI_SOFTCAP) {
             // x <- scale s - slope |i - j| (natural units, before the cap)
 #pragma unroll
-            for (int e = 0; e < 32; e += 2) {
+            for (int e = 0; e < kW; e += 2) {
                 const float b0 = fabsf(static_cast<float>(d0 + e)), b1 = fabsf(static_cast<float>(d0 + e + 1));
                 float s0, s1;
                 fmul2b(s0, s1, x[e], x[e + 1], p.scale, p.scale);
@@ -212,10 +210,10 @@ __device__ __forceinline__ void elem_chunk(const BwdParams& p, int hq, const Ele
         }
         float am = 0.f;
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) am = fmax3(am, fabsf(x[e]), fabsf(x[e + 1]));
+        for (int e = 0; e < kW; e += 2) am = fmax3(am, fabsf(x[e]), fabsf(x[e + 1]));
         const int tier = !__any_sync(0xffffffffu, am > k.xlim2) ? 2 : !__any_sync(0xffffffffu, am > k.xlim4) ? 4 : 0;
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
+        for (int e = 0; e < kW; e += 2) {
             float t0, t1;
             if (tier == 2) {
                 float w0, w1, q0, q1;
@@ -253,7 +251,7 @@ __device__ __forceinline__ void elem_chunk(const BwdParams& p, int hq, const Ele
         }
     } else {
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
+        for (int e = 0; e < kW; e += 2) {
             float a0, a1;
             ffma2(a0, a1, x[e], x[e + 1], k.sl2, k.sl2, nl[e], nl[e + 1]);
             if (SCORE == FA_SCORE_ALIBI) {
@@ -301,7 +299,7 @@ __device__ __forceinline__ bool tc_visible(const BwdParams& p, int b, int i, int
     }
 }
 
-// The visible columns of a 32-column chunk of a partial tile, as a bit mask
+// The visible columns of a kW-column chunk of a partial tile, as a bit mask
 // (bit e: column e).  dK/dV: the row is key j, the columns queries c0 + e;
 // dQ: the row is query i, the columns keys c0 + e.  The closed-form masks
 // leave one interval per row; document and table masks are tested column by
@@ -312,7 +310,7 @@ __device__ __forceinline__ uint32_t chunk_mask(const BwdParams& p, int b, int ro
     if (kind == FA_MASK_DOCUMENT || kind == FA_MASK_TABLE) {
         uint32_t m = 0u;
 #pragma unroll 1
-        for (int e = 0; e < 32; ++e) {
+        for (int e = 0; e < kW; ++e) {
             const bool v = MODE == DKDV ? tc_visible(p, b, c0 + e, row) : tc_visible(p, b, row, c0 + e);
             m |= (v ? 1u : 0u) << e;
         }
@@ -335,7 +333,7 @@ __device__ __forceinline__ uint32_t chunk_mask(const BwdParams& p, int b, int ro
         if (kind == FA_MASK_PREFIX_LM) hi = min(hi, max(i, p.mask.prefix_len - 1) - c0);
     }
     lo = max(lo, 0);
-    hi = min(hi, 31);
+    hi = min(hi, kW - 1);
     if (hi < lo) return 0u;
     return (0xffffffffu >> (31 - hi)) & (0xffffffffu << lo);
 }
@@ -418,14 +416,14 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     if (threadIdx.x == 0) {
         for (int k = 0; k < T_COUNT; ++k) {
             uint32_t cnt = 1;
-            if (k == T_PDS || k == T_PDS + 1 || k == T_ACC_FREE) cnt = 8;
+            if (k == T_PDS || k == T_PDS + 1 || k == T_ACC_FREE) cnt = 16;
             if (k == T_UNIT_EMPTY || k == T_UNIT_EMPTY + 1) cnt = kTcUnitConsumers;
             mbar_init(bar(k), cnt);
         }
         *abort_flag = 0;
         mbar_fence_init();
     }
-    if (warp == 9) {
+    if (warp == kTcMma) {
         tmem_alloc(smem_addr(const_cast<uint32_t*>(tmem_slot)), kTcTmemCols);
         tmem_relinquish();
     }
@@ -437,7 +435,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const uint32_t tX1 = tmem, tX2 = tmem + 128u, tA1 = tmem + 256u, tA2 = tmem + 256u + D;
     const long long rows_pad = (long long)p.B * p.Hq * p.bm.nq * 128;
 
-    if (warp == 8) {
+    if (warp == kTcLoader) {
         // ---------------------------------------------------------- loader
         if (lane == 0) {
             tma_prefetch_desc(&tmQ);
@@ -530,7 +528,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 if (last >= 0 && ls >= 0) tc_drain_wait(bar(T_FULL + s), (ls / ST) & 1, wc, TS_LOAD_DRAIN);
             }
         }
-    } else if (warp == 9) {
+    } else if (warp == kTcMma) {
         // ------------------------------------------------------------- MMA
         constexpr uint32_t idesc_x = idesc_bf16_f32(128, 64, false);
         constexpr uint32_t idesc_a = idesc_bf16_f32(128, D, true);
@@ -554,27 +552,27 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             mma_commit_elect(bar(T_SD + h));
         };
         // dK/dV: A1 += P_h S2_h (dV += P^T dO), A2 += dS_h S1_h (dK += dS^T Q);
-        // dQ: A1 += dS_h S1_h (dQ += dS K).  A from TMEM (bf16: each 32-column
-        // chunk of X1_h / X2_h holds its 32 values in its first 16 columns),
+        // dQ: A1 += dS_h S1_h (dQ += dS K).  A from TMEM (bf16: each 16-column
+        // chunk of X1_h / X2_h holds its 16 values in its first 8 columns),
         // B the half's 64 rows MN-major, K = 64.
         auto issue_acc = [&](int h, int i, bool first) {
             const uint32_t st1 = sbase + L::kRing + (i % ST) * 2 * L::kTile, st2 = st1 + L::kTile;
             const uint64_t m1 = sdesc_sw128(st1 + 8192u * h, 16384, 1024), m2 = sdesc_sw128(st2 + 8192u * h, 16384, 1024);
             // K step kk covers columns 16 kk .. 16 kk + 15 of the half, packed
-            // by chunk (kk >> 1) into its own first 16 TMEM columns
+            // by their chunk kk into its own first 8 TMEM columns
             if (MODE == DKDV) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_ts_elect(tA1, tX1 + 64u * h + 32u * (kk >> 1) + 8u * (kk & 1), m2 + kk * 128u, idesc_a,
+                    mma_ts_elect(tA1, tX1 + 64u * h + 16u * kk, m2 + kk * 128u, idesc_a,
                                  (!first || kk > 0) ? 1u : 0u);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_ts_elect(tA2, tX2 + 64u * h + 32u * (kk >> 1) + 8u * (kk & 1), m1 + kk * 128u, idesc_a,
+                    mma_ts_elect(tA2, tX2 + 64u * h + 16u * kk, m1 + kk * 128u, idesc_a,
                                  (!first || kk > 0) ? 1u : 0u);
             } else {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_ts_elect(tA1, tX2 + 64u * h + 32u * (kk >> 1) + 8u * (kk & 1), m1 + kk * 128u, idesc_a,
+                    mma_ts_elect(tA1, tX2 + 64u * h + 16u * kk, m1 + kk * 128u, idesc_a,
                                  (!first || kk > 0) ? 1u : 0u);
             }
         };
@@ -628,7 +626,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         mma_commit_elect(bar(T_DRAIN));
         tc_drain_wait(bar(T_DRAIN), 0, wc, TS_DRAIN);
         __syncwarp();
-    } else if (warp < 8) {
+    } else if (warp < kTcLoader) {
         // ------------------------------------------------------ elementwise
         const int h = warp >> 2, wq = warp & 3;
         const int r = wq * 32 + lane;
@@ -653,7 +651,6 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         uint32_t k = 0;
         int i = 0, rr = 0, cur_hq = -1;
         bool ok = true;
-        uint8_t* stage = smem + L::kStage + warp * 32 * L::kStageRow;
         while (ok) {
             const uint32_t slot = k & 1;
             if (!mbar_wait_warp(bar(T_UNIT_FULL + slot), (k >> 1) & 1, wc, TS_UNIT_FULL)) break;
@@ -673,10 +670,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             }
             for (int v = 0; v < n && ok; ++v, ++i) {
                 const int s = i % ST;
-                // Both warpgroups work on the same half, warpgroup g on its
-                // chunk g (32 columns); while they turn to the other half, the
-                // tensor pipe runs this half's products and the next visit's
-                // S, dP.
+                // All four warpgroups work on the same half, warpgroup g on
+                // its chunk g (16 columns); while they turn to the other half,
+                // the tensor pipe runs this half's products and the next
+                // visit's S, dP.
 #pragma unroll 1
                 for (int hh = 0; hh < 2; ++hh) {
                     if (!mbar_wait_warp(bar(T_SD + hh), i & 1, wc, TS_SD)) { ok = false; break; }
@@ -689,34 +686,34 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                         cur_hq = hq;
                     }
                     const float* sst = reinterpret_cast<const float*>(smem + L::kStats + s * 1024u);
-                    const int cb = 64 * hh + 32 * h;              // column of the chunk within the tile
+                    const int cb = 64 * hh + kW * h;              // column of the chunk within the tile
                     const int col0 = other * kBlock + cb;         // query (dK/dV) or key (dQ) index of column 0
-                    float x[32], y[32], nl[32], nd[32];
+                    float x[kW], y[kW], nl[kW], nd[kW];
                     {
-                        uint32_t rx[32], ry[32];
-                        tmem_ld32_async(tX1 + lane_off + cb, rx);
-                        tmem_ld32_async(tX2 + lane_off + cb, ry);
+                        uint32_t rx[kW], ry[kW];
+                        tmem_ld16_async(tX1 + lane_off + cb, rx);
+                        tmem_ld16_async(tX2 + lane_off + cb, ry);
                         // the columns' statistics while the loads are in flight
                         if (MODE == DKDV) {
                             const float4* n4 = reinterpret_cast<const float4*>(sst + cb);
                             const float4* d4 = reinterpret_cast<const float4*>(sst + 128 + cb);
 #pragma unroll
-                            for (int q = 0; q < 8; ++q) {
+                            for (int q = 0; q < kW / 4; ++q) {
                                 const float4 a = n4[q], bb = d4[q];
                                 nl[4 * q] = a.x; nl[4 * q + 1] = a.y; nl[4 * q + 2] = a.z; nl[4 * q + 3] = a.w;
                                 nd[4 * q] = bb.x; nd[4 * q + 1] = bb.y; nd[4 * q + 2] = bb.z; nd[4 * q + 3] = bb.w;
                             }
                         } else {
 #pragma unroll
-                            for (int e = 0; e < 32; ++e) {
+                            for (int e = 0; e < kW; ++e) {
                                 nl[e] = nl_row;
                                 nd[e] = nd_row;
                             }
                         }
-                        tmem_wait_ld(rx);
-                        tmem_wait_ld(ry);
+                        tmem_wait_ld16(rx);
+                        tmem_wait_ld16(ry);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) {
+                        for (int e = 0; e < kW; ++e) {
                             x[e] = __uint_as_float(rx[e]);
                             y[e] = __uint_as_float(ry[e]);
                         }
@@ -729,16 +726,16 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                     } else {
                         elem_chunk<SCORE, false>(p, hq, kc, x, y, nl, nd, 0xffffffffu, d0, sgn);
                     }
-                    uint32_t pk[16], dk[16];
+                    uint32_t pk[kW / 2], dk[kW / 2];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
+                    for (int e = 0; e < kW / 2; ++e) {
                         pk[e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
                         dk[e] = pack_bf16x2(y[2 * e], y[2 * e + 1]);
                     }
-                    // P (dK/dV only) and dS into the first 16 columns of the
-                    // chunk's own 32 (read above by this warp only)
-                    if (MODE == DKDV) tmem_st16_nowait(tX1 + lane_off + cb, pk);
-                    tmem_st16_nowait(tX2 + lane_off + cb, dk);
+                    // P (dK/dV only) and dS into the first 8 columns of the
+                    // chunk's own 16 (read above by this warp only)
+                    if (MODE == DKDV) tmem_st8_nowait(tX1 + lane_off + cb, pk);
+                    tmem_st8_nowait(tX2 + lane_off + cb, dk);
                     tmem_wait_st();
                     tc_fence_before();
                     __syncwarp();
@@ -747,79 +744,70 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             }
             if (!ok) break;
             // ------------------------------------------------------ epilogue
-            // dK/dV: warpgroup 0 writes dV (A1), warpgroup 1 dK (A2, times
-            // scale); dQ: warpgroup h writes columns [h D/2, (h + 1) D/2) of
-            // dQ (A1, times scale).  The accumulators are read in one batch,
-            // then released to the next unit (ACC_FREE) before the stores.
-            // Rows past the sequence are not written; a block no visit
-            // reached gets zeros.
+            // dK/dV: warpgroups 0 and 1 write columns [g D/2, (g + 1) D/2) of
+            // dV (A1), warpgroups 2 and 3 those of dK (A2, times scale); dQ:
+            // warpgroup g writes columns [g D/4, (g + 1) D/4) of dQ (A1,
+            // times scale).  The accumulators are read in one batch, then
+            // released to the next unit (ACC_FREE) before the stores, which
+            // go from registers to each thread's own row.  Rows past the
+            // sequence are not written; a block no visit reached gets zeros.
+            constexpr int kCols = MODE == DKDV ? D / 2 : D / 4;     // columns of this warpgroup
+            constexpr int kPieces = kCols / 16;
             float* out;
             uint32_t tacc;
             int col_base, nrows;
             float mul;
             if (MODE == DKDV) {
-                out = (h == 0 ? p.dv : p.dk) + (((size_t)b * p.Hkv + hk) * p.kv_len) * D;
-                tacc = h == 0 ? tA1 : tA2;
-                col_base = 0;
-                mul = h == 0 ? 1.f : DsSign<SCORE>::kValue * p.scale;   // the elementwise step keeps +-dS
+                const bool is_dv = h < 2;
+                out = (is_dv ? p.dv : p.dk) + (((size_t)b * p.Hkv + hk) * p.kv_len) * D;
+                tacc = is_dv ? tA1 : tA2;
+                col_base = (h & 1) * kCols;
+                mul = is_dv ? 1.f : DsSign<SCORE>::kValue * p.scale;   // the elementwise step keeps +-dS
                 nrows = p.kv_len;
             } else {
                 out = p.dq + (((size_t)b * p.Hq + hq0) * p.q_len) * D;
                 tacc = tA1;
-                col_base = h * (D / 2);
+                col_base = h * kCols;
                 mul = DsSign<SCORE>::kValue * p.scale;
                 nrows = p.q_len;
             }
-            constexpr int kCh = MODE == DKDV ? D / 32 : D / 64;     // 32-column chunks of this warp
-            uint32_t acc[kCh][32];
+            uint32_t acc[kPieces][16];
             if (n > 0) {
                 if (!mbar_wait_warp(bar(T_ACC), rr & 1, wc, TS_ACC)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll
-                for (int c = 0; c < kCh; ++c) tmem_ld32_async(tacc + lane_off + col_base + 32u * c, acc[c]);
+                for (int c = 0; c < kPieces; ++c) tmem_ld16_async(tacc + lane_off + col_base + 16u * c, acc[c]);
 #pragma unroll
-                for (int c = 0; c < kCh; ++c) tmem_wait_ld(acc[c]);
+                for (int c = 0; c < kPieces; ++c) tmem_wait_ld16(acc[c]);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(T_ACC_FREE));
                 ++rr;
             } else {
 #pragma unroll
-                for (int c = 0; c < kCh; ++c)
+                for (int c = 0; c < kPieces; ++c)
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) acc[c][e] = 0u;
+                    for (int e = 0; e < 16; ++e) acc[c][e] = 0u;
             }
-            const int rows_left = nrows - (blk * kBlock + wq * 32);
+            if (row < nrows) {
+                float* orow = out + (size_t)row * D + col_base;
 #pragma unroll
-            for (int c = 0; c < 2 * kCh; ++c) {            // 16-column pieces through the staging rows
-                __syncwarp();
+                for (int c = 0; c < kPieces; ++c)
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint32_t* src = &acc[c >> 1][16 * (c & 1) + 4 * q];
-                    *reinterpret_cast<float4*>(stage + lane * L::kStageRow + 16 * q) =
-                        make_float4(__uint_as_float(src[0]) * mul, __uint_as_float(src[1]) * mul,
-                                    __uint_as_float(src[2]) * mul, __uint_as_float(src[3]) * mul);
-                }
-                __syncwarp();
-#pragma unroll
-                for (int it = 0; it < 4; ++it) {
-                    const int rr2 = it * 8 + (lane >> 2), piece = lane & 3;
-                    if (rr2 < rows_left) {
-                        const float4 val = *reinterpret_cast<const float4*>(stage + rr2 * L::kStageRow + 16 * piece);
-                        const size_t grow = (size_t)(blk * kBlock + wq * 32 + rr2);
-                        *reinterpret_cast<float4*>(out + grow * D + col_base + 16 * c + 4 * piece) = val;
-                    }
-                }
+                    for (int q = 0; q < 4; ++q)
+                        *reinterpret_cast<float4*>(orow + 16 * c + 4 * q) =
+                            make_float4(__uint_as_float(acc[c][4 * q]) * mul, __uint_as_float(acc[c][4 * q + 1]) * mul,
+                                        __uint_as_float(acc[c][4 * q + 2]) * mul, __uint_as_float(acc[c][4 * q + 3]) * mul);
             }
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == kTcMma) {
         tc_fence_after();
         tmem_dealloc(tmem, kTcTmemCols);
     }
-    if (threadIdx.x == 256 + 32 && p.ws) {
+    if (threadIdx.x == 32 * kTcMma && p.ws) {
         // The last CTA out resets the unit counter for the next launch on
         // the same workspace (the dQ kernel, or the next backward).
         __threadfence();
