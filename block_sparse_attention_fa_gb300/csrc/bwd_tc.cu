@@ -212,27 +212,35 @@ __device__ __forceinline__ void elem_chunk(const BwdParams& p, int hq, const Ele
 #pragma unroll
         for (int e = 0; e < kW; e += 2) am = fmax3(am, fabsf(x[e]), fabsf(x[e + 1]));
         const int tier = !__any_sync(0xffffffffu, am > k.xlim2) ? 2 : !__any_sync(0xffffffffu, am > k.xlim4) ? 4 : 0;
+        // x <- t = tanh(ci x), in place; only this part depends on the tier,
+        // so that the rest of the step is one copy of code
+        if (tier == 2) {
 #pragma unroll
-        for (int e = 0; e < kW; e += 2) {
-            float t0, t1;
-            if (tier == 2) {
+            for (int e = 0; e < kW; e += 2) {
                 float w0, w1, q0, q1;
                 fmul2b(w0, w1, x[e], x[e + 1], x[e], x[e + 1]);
                 ffma2(q0, q1, w0, w1, k.r2, k.r2, k.r1, k.r1);
                 ffma2(q0, q1, q0, q1, w0, w1, k.r0, k.r0);
-                fmul2b(t0, t1, x[e], x[e + 1], q0, q1);
-            } else if (tier == 4) {
+                fmul2b(x[e], x[e + 1], x[e], x[e + 1], q0, q1);
+            }
+        } else if (tier == 4) {
+#pragma unroll
+            for (int e = 0; e < kW; e += 2) {
                 float w0, w1, q0, q1;
                 fmul2b(w0, w1, x[e], x[e + 1], x[e], x[e + 1]);
                 ffma2(q0, q1, w0, w1, k.q4, k.q4, k.q3, k.q3);
                 ffma2(q0, q1, q0, q1, w0, w1, k.q2, k.q2);
                 ffma2(q0, q1, q0, q1, w0, w1, k.q1, k.q1);
                 ffma2(q0, q1, q0, q1, w0, w1, k.q0, k.q0);
-                fmul2b(t0, t1, x[e], x[e + 1], q0, q1);
-            } else {
-                t0 = tanh_exact(x[e] * k.ci);
-                t1 = tanh_exact(x[e + 1] * k.ci);
+                fmul2b(x[e], x[e + 1], x[e], x[e + 1], q0, q1);
             }
+        } else {
+#pragma unroll
+            for (int e = 0; e < kW; ++e) x[e] = tanh_exact(x[e] * k.ci);
+        }
+#pragma unroll
+        for (int e = 0; e < kW; e += 2) {
+            const float t0 = x[e], t1 = x[e + 1];
             float a0, a1;
             ffma2(a0, a1, t0, t1, k.cap_out, k.cap_out, nl[e], nl[e + 1]);
             float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
