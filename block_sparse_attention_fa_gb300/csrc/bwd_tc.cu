@@ -90,7 +90,13 @@ struct TcLayout {
     static constexpr uint32_t kBars = kUnitQ + 2 * 4 * TU_WORDS;
     static constexpr uint32_t kTmemSlot = kBars + 8 * T_COUNT;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
-    static constexpr uint32_t kUsed = kAbort + 12;
+    // epilogue staging: per elementwise warp 8 rows x 32 floats, rows padded
+    // to 36 floats so that 8 lanes writing one 16-byte piece each of their
+    // own rows hit 32 different banks
+    static constexpr uint32_t kEpiRow = 36 * 4, kEpiWarp = 8 * kEpiRow;
+    static constexpr uint32_t kEpi = (kAbort + 12 + 15) & ~15u;
+    static constexpr uint32_t kUsed = kEpi + 16 * kEpiWarp;
+    static_assert(kEpi % 16 == 0 && kEpiRow % 16 == 0, "float4 staging");
     static constexpr uint32_t kDynamic = kUsed + 1024;          // + 1 KB to align the base to 1024
     static_assert(kDynamic <= 227u * 1024u, "shared memory budget");
     static_assert(kStages <= kMaxSt, "too many stages");
@@ -605,6 +611,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             // much larger (the forward's MMA warps gained 11 % from the same).
 #pragma unroll 1
             for (int h = 0; h < 2; ++h) issue_x(h, i);
+            // R1, R2 are read by the S, dP products only: once the unit's
+            // last ones are issued, the commit frees them for the next unit's
+            // resident tiles, which then load during the last visit
+            if (n == 1) mma_commit_elect(bar(T_R_EMPTY));
             for (int v = 0; v < n && ok; ++v, ++i) {
                 const bool more = v + 1 < n;
 #pragma unroll 1
@@ -622,8 +632,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                             tc_fence_after();
                         }
                         issue_x(h, i + 1);
-                    } else if (h == 1) {
-                        mma_commit_elect(bar(T_R_EMPTY));     // every product reading R1, R2 is issued
+                        if (h == 1 && v + 2 == n) mma_commit_elect(bar(T_R_EMPTY));
                     }
                 }
             }
@@ -755,12 +764,16 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             // dK/dV: warpgroups 0 and 1 write columns [g D/2, (g + 1) D/2) of
             // dV (A1), warpgroups 2 and 3 those of dK (A2, times scale); dQ:
             // warpgroup g writes columns [g D/4, (g + 1) D/4) of dQ (A1,
-            // times scale).  The accumulators are read in one batch, then
-            // released to the next unit (ACC_FREE) before the stores, which
-            // go from registers to each thread's own row.  Rows past the
+            // times scale).  Per segment of up to 32 columns each warp reads
+            // its 32 rows from TMEM (the last segment's read releases the
+            // accumulators to the next unit, ACC_FREE) and passes them through
+            // its staging rows 8 at a time, so that a store instruction writes
+            // whole 128-byte lines (four rows of 32 columns) rather than 32
+            // rows' 16-byte pieces.  Rows past the
             // sequence are not written; a block no visit reached gets zeros.
             constexpr int kCols = MODE == DKDV ? D / 2 : D / 4;     // columns of this warpgroup
-            constexpr int kPieces = kCols / 16;
+            constexpr int kSeg = kCols < 32 ? kCols : 32;            // columns per staged segment
+            constexpr int kQ = kSeg / 4;                             // float4 per staged row
             float* out;
             uint32_t tacc;
             int col_base, nrows;
@@ -779,33 +792,59 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 mul = DsSign<SCORE>::kValue * p.scale;
                 nrows = p.q_len;
             }
-            uint32_t acc[kPieces][16];
             if (n > 0) {
                 if (!mbar_wait_warp(bar(T_ACC), rr & 1, wc, TS_ACC)) { ok = false; break; }
                 tc_fence_after();
-#pragma unroll
-                for (int c = 0; c < kPieces; ++c) tmem_ld16_async(tacc + lane_off + col_base + 16u * c, acc[c]);
-#pragma unroll
-                for (int c = 0; c < kPieces; ++c) tmem_wait_ld16(acc[c]);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(T_ACC_FREE));
                 ++rr;
-            } else {
-#pragma unroll
-                for (int c = 0; c < kPieces; ++c)
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) acc[c][e] = 0u;
             }
-            if (row < nrows) {
-                float* orow = out + (size_t)row * D + col_base;
+            float* stg = reinterpret_cast<float*>(smem + L::kEpi + warp * L::kEpiWarp);
+            const int row0 = blk * kBlock + wq * 32;                 // first row of this warp
+#pragma unroll 1
+            for (int c0 = 0; c0 < kCols; c0 += kSeg) {
+                // this segment's accumulator columns; after the last segment's
+                // loads the accumulators go back to the MMA warp
+                uint32_t acc[kSeg / 16][16];
+                if (n > 0) {
 #pragma unroll
-                for (int c = 0; c < kPieces; ++c)
+                    for (int c = 0; c < kSeg / 16; ++c) tmem_ld16_async(tacc + lane_off + col_base + c0 + 16u * c, acc[c]);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        *reinterpret_cast<float4*>(orow + 16 * c + 4 * q) =
-                            make_float4(__uint_as_float(acc[c][4 * q]) * mul, __uint_as_float(acc[c][4 * q + 1]) * mul,
-                                        __uint_as_float(acc[c][4 * q + 2]) * mul, __uint_as_float(acc[c][4 * q + 3]) * mul);
+                    for (int c = 0; c < kSeg / 16; ++c) tmem_wait_ld16(acc[c]);
+                    if (c0 + kSeg == kCols) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar(T_ACC_FREE));
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < kSeg / 16; ++c)
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) acc[c][e] = 0u;
+                }
+#pragma unroll 1
+                for (int g = 0; g < 4; ++g) {
+                    // lanes 8 g .. 8 g + 7 put their rows' segment into the staging rows
+                    if ((lane >> 3) == g) {
+                        float* dst = stg + (lane & 7) * (L::kEpiRow / 4);
+#pragma unroll
+                        for (int q = 0; q < kQ; ++q) {
+                            const uint32_t* a = &acc[q >> 2][4 * (q & 3)];
+                            *reinterpret_cast<float4*>(dst + 4 * q) =
+                                make_float4(__uint_as_float(a[0]) * mul, __uint_as_float(a[1]) * mul,
+                                            __uint_as_float(a[2]) * mul, __uint_as_float(a[3]) * mul);
+                        }
+                    }
+                    __syncwarp();
+                    // the 8 rows to global memory, 32 float4 per instruction
+#pragma unroll
+                    for (int k2 = 0; k2 < 8 * kQ / 32; ++k2) {
+                        const int idx = 32 * k2 + lane, rw = idx / kQ, cq = idx % kQ;
+                        const int grow = row0 + 8 * g + rw;
+                        const float4 val = *reinterpret_cast<const float4*>(stg + rw * (L::kEpiRow / 4) + 4 * cq);
+                        if (grow < nrows)
+                            *reinterpret_cast<float4*>(out + (size_t)grow * D + col_base + c0 + 4 * cq) = val;
+                    }
+                    __syncwarp();
+                }
             }
         }
     }
