@@ -604,6 +604,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             if (n == 0) continue;
             if (!mbar_wait_warp(bar(T_R_FULL), rr & 1, wc, TS_R)) break;
             if (!mbar_wait_warp(bar(T_FULL + i % ST), (i / ST) & 1, wc, TS_FULL)) break;
+            // the previous unit's accumulators have been read: its epilogue's
+            // TMEM loads then do not queue behind this unit's first products
+            if (rr > 0 && !mbar_wait_warp(bar(T_ACC_FREE), (rr - 1) & 1, wc, TS_ACC_FREE)) break;
             tc_fence_after();
             // The halves are rolled loops: the warp shares its SM
             // sub-partition's instruction cache with elementwise warps, and a
@@ -620,8 +623,6 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 #pragma unroll 1
                 for (int h = 0; h < 2; ++h) {
                     if (!mbar_wait_warp(bar(T_PDS + h), i & 1, wc, TS_PDS)) { ok = false; break; }
-                    if (v == 0 && h == 0 && rr > 0 &&
-                        !mbar_wait_warp(bar(T_ACC_FREE), (rr - 1) & 1, wc, TS_ACC_FREE)) { ok = false; break; }
                     tc_fence_after();
                     issue_acc(h, i, v == 0 && h == 0);
                     if (h == 1) mma_commit_elect(bar(T_EMPTY + i % ST));
