@@ -694,8 +694,29 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 // visit's S, dP.
 #pragma unroll 1
                 for (int hh = 0; hh < 2; ++hh) {
-                    if (!mbar_wait_warp(bar(T_SD + hh), i & 1, wc, TS_SD)) { ok = false; break; }
                     if (hh == 0 && !mbar_wait_warp(bar(T_FULL + s), (i / ST) & 1, wc, TS_FULL_E)) { ok = false; break; }
+                    const float* sst = reinterpret_cast<const float*>(smem + L::kStats + s * 1024u);
+                    const int cb = 64 * hh + kW * h;              // column of the chunk within the tile
+                    // the columns' statistics (in the stage since FULL), read
+                    // while S_h, dP_h are still being computed
+                    float nl[kW], nd[kW];
+                    if (MODE == DKDV) {
+                        const float4* n4 = reinterpret_cast<const float4*>(sst + cb);
+                        const float4* d4 = reinterpret_cast<const float4*>(sst + 128 + cb);
+#pragma unroll
+                        for (int q = 0; q < kW / 4; ++q) {
+                            const float4 a = n4[q], bb = d4[q];
+                            nl[4 * q] = a.x; nl[4 * q + 1] = a.y; nl[4 * q + 2] = a.z; nl[4 * q + 3] = a.w;
+                            nd[4 * q] = bb.x; nd[4 * q + 1] = bb.y; nd[4 * q + 2] = bb.z; nd[4 * q + 3] = bb.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < kW; ++e) {
+                            nl[e] = nl_row;
+                            nd[e] = nd_row;
+                        }
+                    }
+                    if (!mbar_wait_warp(bar(T_SD + hh), i & 1, wc, TS_SD)) { ok = false; break; }
                     tc_fence_after();
                     const int other = info[4 * s + 0], hq = info[4 * s + 1];
                     const bool partial = info[4 * s + 2] != 0;
@@ -703,31 +724,12 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                         kc.slope = __ldg(p.score.slopes + hq) * (SCORE == FA_SCORE_ALIBI ? kLog2eT : 1.f);
                         cur_hq = hq;
                     }
-                    const float* sst = reinterpret_cast<const float*>(smem + L::kStats + s * 1024u);
-                    const int cb = 64 * hh + kW * h;              // column of the chunk within the tile
                     const int col0 = other * kBlock + cb;         // query (dK/dV) or key (dQ) index of column 0
-                    float x[kW], y[kW], nl[kW], nd[kW];
+                    float x[kW], y[kW];
                     {
                         uint32_t rx[kW], ry[kW];
                         tmem_ld16_async(tX1 + lane_off + cb, rx);
                         tmem_ld16_async(tX2 + lane_off + cb, ry);
-                        // the columns' statistics while the loads are in flight
-                        if (MODE == DKDV) {
-                            const float4* n4 = reinterpret_cast<const float4*>(sst + cb);
-                            const float4* d4 = reinterpret_cast<const float4*>(sst + 128 + cb);
-#pragma unroll
-                            for (int q = 0; q < kW / 4; ++q) {
-                                const float4 a = n4[q], bb = d4[q];
-                                nl[4 * q] = a.x; nl[4 * q + 1] = a.y; nl[4 * q + 2] = a.z; nl[4 * q + 3] = a.w;
-                                nd[4 * q] = bb.x; nd[4 * q + 1] = bb.y; nd[4 * q + 2] = bb.z; nd[4 * q + 3] = bb.w;
-                            }
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < kW; ++e) {
-                                nl[e] = nl_row;
-                                nd[e] = nd_row;
-                            }
-                        }
                         tmem_wait_ld16(rx);
                         tmem_wait_ld16(ry);
 #pragma unroll
