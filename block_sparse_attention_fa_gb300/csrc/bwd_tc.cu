@@ -801,8 +801,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             // accumulators to the next unit, ACC_FREE) and passes them through
             // its staging rows 8 at a time, so that a store instruction writes
             // whole 128-byte lines (four rows of 32 columns) rather than 32
-            // rows' 16-byte pieces.  Rows past the
-            // sequence are not written; a block no visit reached gets zeros.
+            // rows' 16-byte pieces.  Rows past the sequence are not written;
+            // a block no visit reached gets zeros.
             constexpr int kCols = MODE == DKDV ? D / 2 : D / 4;     // columns of this warpgroup
             constexpr int kSeg = kCols < 32 ? kCols : 32;            // columns per staged segment
             constexpr int kQ = kSeg / 4;                             // float4 per staged row
